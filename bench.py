@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Throughput of the batched verification step on one GB300.
+
+A step is one pass of the whole hot path over one batch: row statistics of
+every verified target and draft row, AV scoring, the left-to-right
+acceptance scan, residual/bonus sampling, and one AV refit step (for the
+AV-truncated canvas workload also the AV scoring call that trims the canvas
+first).  Inputs are seeded synthetic logits resident in HBM; each step uses
+its own Philox seed.  The default workload is B=256, K=5, V=128256 bf16
+(722 MB of logits per step, larger than the 129 MB L2, so no flush is
+needed between steps).
+
+Prints ONE JSON line.  `--impl reference` times the CPU oracle instead (the
+only reference this path has), on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/sec (B·(K+1)) and achieved HBM GB/s vs GB300 peak, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "c2": dict(B=64, K=4, V=32000, desc="B=64 K=4 V=32000 bf16, z~N(0,3^2) +8 on one token, draft=z+N(0,1), "
+               "tau=1, AV on (omega=1, beta=0), one refit per step"),
+    "c3": dict(B=256, K=5, V=128256, desc="B=256 K=5 V=128256 bf16, z~N(0,3^2) with a peaked top token, "
+               "draft=0.8z+N(0,1.5^2) (alpha~0.7), tau=1, AV scoring + one refit per step"),
+    "c4": dict(B=1024, K=7, V=151936, desc="B=1024 K=7 V=151936 bf16, draft noise sigma_b~U(0.5,3), "
+               "tau~U(0.3,1.2), 10% greedy rows, AV scoring + one refit per step"),
+    "c5": dict(B=512, K=16, V=128256, desc="B=512 K<=16 V=128256 bf16, AV-truncated canvas (survival >= 0.3), "
+               "draft noise 0.5+0.2i, scoring + verify on the kept canvas + one refit per step"),
+}
+
+
+def _peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_03_gb300", "csrc")
+    for fn in ("rowpass.cu", "sv_device.cuh", "sv_internal.h"):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload):
+    """DRAM bytes per row-pass launch from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "rowpass_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_sha") != _kernel_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], samples=0)
+        sm.sort()
+        return dict(sm_mhz=sm[len(sm) // 2], sm_max_mhz=max(mx), reasons=sorted(reasons), samples=len(sm))
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _bytes_per_step(wl, K, V, esz, kept, accept):
+    """Algorithmic bytes of one step.  Returns (bytes of the row-pass launch
+    that the launch events bracket, all bytes of the step).  The step reads
+    every verified target row (k_b + 1) and draft row (k_b) once, re-reads
+    the residual or bonus target row (+ the draft row when rejected), and
+    moves 4 B (3K + 4) of small per-sequence inputs and outputs.  On the
+    AV-truncated canvas the scoring call reads all K draft rows, and the
+    verify row pass (the bracketed one) then reads only the k_b + 1 target
+    rows."""
+    B = kept.size
+    second = int(B + (accept < kept).sum()) * V * esz
+    small = 4 * B * (3 * K + 4)
+    if wl == "c5":
+        bracketed = int((kept + 1).sum()) * V * esz
+        first = bracketed + B * K * V * esz
+    else:
+        bracketed = first = int((2 * kept + 1).sum()) * V * esz
+    return bracketed, first + second + small
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from speculative_decoding_verification_03_gb300 import binding, synth
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    binding.lib()  # fails loudly if the library was not built
+    cfg = WORKLOADS[args.workload]
+    B, K, V = cfg["B"], cfg["K"], cfg["V"]
+    w = getattr(synth, args.workload)(seed=rank, device=dev)
+    theta0 = [1.0] + [0.0] * K if args.workload != "c5" else [0.55] + [0.9 - 0.15 * i for i in range(K)]
+    theta = torch.tensor(theta0, dtype=torch.float32, device=dev)
+    ws = binding.workspace(B, K, V, dev)
+    state = binding.AVState(K, device=dev)
+    out = dict(tokens=torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+               accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
+               feature=torch.empty((B, K), dtype=torch.float32, device=dev),
+               conf=torch.empty((B, K), dtype=torch.float32, device=dev))
+    score = None
+    if args.workload == "c5":
+        score = dict(feature=torch.empty((B, K), dtype=torch.float32, device=dev),
+                     conf=torch.empty((B, K), dtype=torch.float32, device=dev),
+                     kept_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                     stats=torch.empty((B, K, 4), dtype=torch.int32, device=dev))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, record=None):
+        if score is not None:
+            binding.av_score(w.draft, w.temperature, theta, keep_threshold=0.3, want_stats=True, ws=ws, out=score)
+            binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, i, draft_len=score["kept_len"],
+                           theta=theta, draft_stats=score["stats"], want_feature=True, ws=ws, out=out)
+            state.fit_step(theta, out["feature"], out["accept_len"], score["kept_len"])
+        else:
+            binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, i, theta=theta, want_feature=True,
+                           ws=ws, out=out)
+            state.fit_step(theta, out["feature"], out["accept_len"])
+        if record is not None:
+            record.append((out["accept_len"].clone(), None if score is None else score["kept_len"].clone()))
+
+    for i in range(args.warmup):
+        step(10**6 + i)
+    rc, flags = binding.status(ws)
+    if rc != 0:
+        raise SystemExit("device status %d (flags %#x) after warm-up" % (rc, flags))
+
+    # per-step events around the row-pass kernel (the dominant kernel)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        b.record(stream)
+    outcomes = []
+    clocks = Clocks(local) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        binding.set_launch_events(*ev[i])
+        step(i, outcomes)
+    binding.set_launch_events(None, None)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    elapsed_ms = t0.elapsed_time(t1)
+    rowpass_ms = [a.elapsed_time(b) for a, b in ev]
+    rc, flags = binding.status(ws)
+    if rc != 0:
+        raise SystemExit("device status %d (flags %#x) in the timed region" % (rc, flags))
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    # work done: verified rows (sum over sequences of k_b + 1) and algorithmic bytes
+    esz = w.target.element_size()
+    rows, bytes_rp, bytes_all = 0, 0, 0
+    for acc, kept in outcomes:
+        a = acc.cpu().numpy()
+        k = np.full(B, K) if kept is None else kept.cpu().numpy()
+        f, t = _bytes_per_step(args.workload, K, V, esz, k, a)
+        rows += int((k + 1).sum())
+        bytes_rp += f
+        bytes_all += t
+    value = rows * world / (elapsed_ms / 1e3)
+    launches_per_step = 3 + (1 if score is not None else 0)
+
+    res = dict(metric=METRIC, value=value, unit="rows/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+               ms_per_step=elapsed_ms / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
+               dtype="f32", data="synthetic (seeded; stands in for the pages' model pairs and datasets)")
+    peak, peak_kind = _peak()
+    # on the AV-truncated canvas both row passes of a step record the same
+    # event pair; the later (verify) launch is the one that stays bracketed
+    rp_ms = sum(rowpass_ms) / len(rowpass_ms)
+    rp_bytes = bytes_rp / args.steps
+    achieved = rp_bytes / (rp_ms / 1e3) / 1e9
+    res["roofline"] = dict(bound="hbm", kernel="rowpass_kernel", achieved=achieved, peak=peak, unit="GB/s",
+                           frac=achieved / peak, peak_source="%s (MEASURED_PEAKS hbm_gbs)" % peak_kind
+                           if peak_kind == "measured" else "fallback 6.8 TB/s",
+                           traffic=_traffic(args.workload), algorithmic_bytes_per_launch=rp_bytes,
+                           ms_per_launch=rp_ms)
+    res["step_hbm"] = dict(algorithmic_bytes_per_step=bytes_all / args.steps,
+                           achieved_gbs=bytes_all / args.steps / (elapsed_ms / args.steps / 1e3) / 1e9)
+    res["gpu_launches"] = launches_per_step * args.steps
+    res["clocks"] = clk
+    res["config"] = dict(workload=args.workload + ": " + cfg["desc"], B=B, K=K, V=V, logits="bf16",
+                         global_batch=B * world, l2="inputs %.0f MB per step > 129 MB L2: no flush" %
+                         (w.bytes_first_pass() / 1e6), parallelism="replicas" if world > 1 else "single GPU")
+    if rank == 0 and world == 1 and not args.no_e2e:
+        res["e2e"] = run_e2e(args, w, theta0, dev)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        res["cpu_baseline"] = cpu_baseline(args, budget_s=args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def run_e2e(args, w, theta0, dev, steps=None):
+    """Same metric through the public API with host buffers: each step copies
+    its inputs from pinned host memory, verifies, refits, and reads the
+    emitted tokens and accept lengths back."""
+    import torch
+
+    from speculative_decoding_verification_03_gb300 import binding
+
+    steps = steps or min(args.steps, 20)
+    B, K, V = w.B, w.K, w.V
+    host = dict(target=w.target.cpu().pin_memory(), draft=w.draft.cpu().pin_memory(),
+                draft_tokens=w.draft_tokens.cpu().pin_memory(), temperature=w.temperature.cpu().pin_memory())
+    tok_h = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    acc_h = torch.empty((B,), dtype=torch.int32).pin_memory()
+    sess = binding.HostSession(B, K, V, w.dtype, dev, theta0)
+    for i in range(2):
+        sess.step(host, i, tok_h, acc_h)
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    s = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(steps):
+        sess.step(host, i, tok_h, acc_h)
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = tok_h.numel() * 4 + acc_h.numel() * 4
+    return dict(value=B * (K + 1) * steps / (ms / 1e3), unit="rows/s", h2d_bytes_per_step=h2d,
+                d2h_bytes_per_step=d2h, steps=steps, wall_s=time.perf_counter() - t)
+
+
+def cpu_baseline(args, budget_s=12.0, max_seqs=None):
+    """The oracle as it stands, single-threaded, on sequences of the same
+    workload until about budget_s seconds of CPU work."""
+    import numpy as np
+
+    import oracle
+    from speculative_decoding_verification_03_gb300 import synth
+
+    cfg = WORKLOADS[args.workload]
+    B, K, V = cfg["B"], cfg["K"], cfg["V"]
+    n = 4 if args.workload != "c4" else 2
+    w = getattr(synth, args.workload)(seed=0, B=max(n, 2), device="cpu")
+    th = np.array([1.0] + [0.0] * K)
+    tgt, drf = synth.logits_np(w.target), synth.logits_np(w.draft)
+    toks, tau = w.draft_tokens.numpy(), w.temperature.numpy()
+    done_rows, done_seqs, t0 = 0, 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and (max_seqs is None or done_seqs < max_seqs):
+        r = oracle.verify(tgt, drf, toks, tau, done_seqs, theta=th)
+        fit = oracle.AVFit(th)
+        fit.step(r["feature"], r["accept_len"])
+        done_rows += int(w.B * (K + 1))
+        done_seqs += w.B
+    dt = time.perf_counter() - t0
+    return dict(value=done_rows / dt, unit="rows/s", cores=1, kind="oracle",
+                sample="%d sequences of the %s workload (B=%d, K=%d, V=%d), oracle verify + refit, %.1f s"
+                % (done_seqs, args.workload, B, K, V, dt))
+
+
+# --------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    import numpy as np
+
+    import oracle
+    from speculative_decoding_verification_03_gb300 import synth
+
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    oracle.build()
+    cfg = WORKLOADS[args.workload]
+    B, K, V = cfg["B"], cfg["K"], cfg["V"]
+    # size each step's sample so that warm-up + steps take about two minutes
+    w = getattr(synth, args.workload)(seed=0, B=8, device="cpu")
+    tgt, drf = synth.logits_np(w.target), synth.logits_np(w.draft)
+    toks, tau = w.draft_tokens.numpy(), w.temperature.numpy()
+    th = np.array([1.0] + [0.0] * K)
+    t = time.perf_counter()
+    oracle.verify(tgt[:1], drf[:1], toks[:1], tau[:1], 0, theta=th)
+    per_seq = time.perf_counter() - t
+    n = int(max(1, min(8, 120.0 / max(1, args.steps + args.warmup) / per_seq)))
+
+    def step(i):
+        sl = slice((i * n) % (8 - n + 1), (i * n) % (8 - n + 1) + n)
+        r = oracle.verify(tgt[sl], drf[sl], toks[sl], tau[sl], i, theta=th)
+        fit = oracle.AVFit(th)
+        fit.step(r["feature"], r["accept_len"])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = n * (K + 1) * args.steps / dt
+    sample = "%d of %d sequences per step (%s workload, V=%d), oracle verify + refit, 1 thread" % (
+        n, B, args.workload, V)
+    res = dict(impl="reference", metric=METRIC, value=value, unit="rows/s", n_gpus=world, steps=args.steps,
+               warmup=args.warmup, ms_per_step=dt / args.steps * 1e3, higher_is_better=True, scaling="weak",
+               vs_baseline=None, dtype="f64", data="synthetic",
+               config=dict(workload=args.workload + ": " + cfg["desc"], B=B, K=K, V=V, logits="bf16"),
+               cpu_baseline=dict(value=value, unit="rows/s", cores=1, kind="oracle", sample=sample),
+               e2e=dict(value=value, unit="rows/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c3")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+/*
+ * specverify -- batched speculative-decoding verification with the
+ * Adaptive-Verification (AV) acceptance estimator, for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only; no CUDA or framework types.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Device pointers point to memory of the current CUDA device; the caller
+ *    owns every buffer (inputs, outputs, workspace, AV state).  The library
+ *    never allocates and never frees.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every call only enqueues work on it and returns without
+ *    waiting; only sv_status() synchronises.
+ *  - Arguments the host can check (sizes, NULL pointers, alignment, workspace
+ *    size) are checked before anything is enqueued; a failed check returns an
+ *    error and enqueues nothing.
+ *  - Conditions only the GPU can see (NaN logits, out-of-range drafted tokens,
+ *    draft_len outside [0, K], negative temperatures, a wait that timed out)
+ *    set bits of a 32-bit status word held in the first 4 bytes of the
+ *    workspace (or of the AV state); sv_status() reads and clears it.  A call
+ *    that uses a workspace clears its status word first, so the word reports
+ *    the most recent call; the AV state's word accumulates across refit steps
+ *    until it is read.  The
+ *    kernels never trap: the affected sequence still gets outputs, produced
+ *    by the rules stated at each flag.
+ *  - Logits are row-major, the vocabulary innermost and contiguous.  Any
+ *    V in [1, SV_MAX_V] is accepted; rows need not be 16-byte aligned (the
+ *    ragged ends are read with plain loads), but each logit pointer must be
+ *    aligned to its element size.
+ *
+ * Notation (as in the AV article): p = target (verifier) distribution,
+ * q = draft distribution.  B sequences, K drafted tokens each, vocabulary V.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SV_MAX_K 16
+#define SV_MAX_V (1 << 24)
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID = 1,      /* a host-checkable argument is wrong              */
+    SV_ERR_UNSUPPORTED = 2,  /* device is not sm_103 / feature not available    */
+    SV_ERR_CUDA = 3,         /* a CUDA runtime call failed                      */
+    SV_ERR_NONFINITE = 4,    /* device: NaN in a row, or a row's max not finite */
+    SV_ERR_TOKEN_RANGE = 5,  /* device: a drafted token outside [0, V)          */
+    SV_ERR_TIMEOUT = 6,      /* device: a bounded wait gave up                  */
+    SV_ERR_WORKSPACE = 7,    /* workspace (or AV state) too small or misaligned */
+    SV_ERR_BAD_LEN = 8,      /* device: draft_len[b] outside [0, K]             */
+    SV_ERR_BAD_TEMP = 9      /* device: temperature[b] negative or NaN          */
+} sv_status_t;
+
+typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype_t;
+
+/* Bits of the device status word (sv_status maps them to sv_status_t). */
+#define SV_FLAG_NONFINITE      (1u << 0)
+#define SV_FLAG_TOKEN_RANGE    (1u << 1)
+#define SV_FLAG_TIMEOUT        (1u << 2)
+#define SV_FLAG_BAD_LEN        (1u << 3)
+#define SV_FLAG_BAD_TEMP       (1u << 4)
+#define SV_FLAG_ZERO_RESIDUAL  (1u << 5) /* warning only: residual mass 0 by rounding, p sampled */
+#define SV_FLAG_FIT_SINGULAR   (1u << 6) /* warning only: refit system not positive definite, theta kept */
+
+/* Softmax statistics of one vocabulary row, 16 bytes.
+ *   m      max_v z_v of the raw logits (before the temperature)
+ *   E      sum over v != argmax of exp((z_v - m) / tau)  (exactly one copy of
+ *          the max excluded); so S = 1 + E, ln S = log1p(E), q_max = 1 / S,
+ *          logit(q_max) = -ln E
+ *   argmax lowest index attaining m
+ *   flags  SV_FLAG_* bits seen on this row
+ * Greedy rows (tau == 0) are summarised at tau = 1. */
+typedef struct {
+    float m;
+    float E;
+    int32_t argmax;
+    uint32_t flags;
+} sv_row_stats_t;
+
+/* ------------------------------------------------------------------------
+ * sv_workspace_bytes -- size of the scratch buffer sv_verify and sv_av_score
+ * need for this shape (row statistics, per-call counters, sampling partial
+ * sums, status word).  The buffer must be 256-byte aligned.  Its contents
+ * need no initialisation: each call clears what it uses on `stream`.  Calls
+ * that share one workspace must be ordered (same stream, or events).
+ * Returns 0 for an invalid shape.
+ * ---------------------------------------------------------------------- */
+size_t sv_workspace_bytes(int B, int K, int V);
+
+/* ------------------------------------------------------------------------
+ * sv_verify -- one batched verification step.
+ *
+ * Defined by "Speculative Decoding: Draft, EAGLE, MTP" (cheatsheet), section
+ * "one speculative step" and its "algorithm loop in code": drafts d_i are
+ * accepted left to right with probability min(1, p_i(d_i) / q_i(d_i)); at
+ * the first rejection a token is drawn from the normalised positive residual
+ * max(p_a - q_a, 0); if every verified draft is accepted a bonus token is
+ * drawn from the next target row.  With theta != NULL the AV score of every
+ * verified draft is computed in the same pass ("Adaptive Verification
+ * without a confidence head", sections "Solution" and "Scoring the
+ * distribution"): x_i = logit(q_max) of draft row i, conf_i =
+ * sigmoid(omega * x_i + beta_i).
+ *
+ *   B, K, V         sequences, drafts per sequence (0..SV_MAX_K), vocabulary
+ *   dtype           SV_BF16 or SV_FP32 logits
+ *   target_logits   device [B][K+1][V]; row j = target logits at draft
+ *                   position j (row K follows the last draft)
+ *   draft_logits    device [B][K][V] (required when K > 0; with draft_stats
+ *                   only the residual rows are read from it)
+ *   draft_tokens    device int32 [B][K], the drafted tokens
+ *   draft_len       device int32 [B] or NULL (= K): k_b drafts of sequence b
+ *                   are verified; target rows j > k_b and draft rows i >= k_b
+ *                   are not read.  Out-of-range values set SV_FLAG_BAD_LEN and
+ *                   are clamped to [0, K].
+ *   temperature     device float [B]; tau_b > 0 divides both rows' logits;
+ *                   0 makes the row greedy: draft i is accepted iff it equals
+ *                   the target argmax of row i (lowest index on ties) and the
+ *                   emitted token is that argmax; no uniforms are drawn.
+ *                   Negative or NaN values set SV_FLAG_BAD_TEMP and act as 0.
+ *   seed            Philox4x32-10 key.  Acceptance at position i uses
+ *                   U(seed, b, i, 0); the residual/bonus draw at position a
+ *                   uses U(seed, b, a, 1), where U(seed, b, pos, draw) is the
+ *                   top 24 bits of output word (draw % 4) of Philox4x32-10
+ *                   with key (seed & 0xffffffff, seed >> 32) and counter
+ *                   (b, pos, draw / 4, 0), times 2^-24.
+ *   theta           device float [K+1] (omega, beta_0..beta_{K-1}) or NULL
+ *   draft_stats     device [B][K] statistics from sv_av_score, or NULL: when
+ *                   given, draft rows are not re-read for their statistics
+ *   out_tokens      device int32 [B][K+1]: accepted drafts, then the
+ *                   residual/bonus token, then -1
+ *   out_accept_len  device int32 [B]: number of accepted drafts a_b
+ *   out_feature     device float [B][K] or NULL: x_i for i < k_b, NaN beyond
+ *   out_conf        device float [B][K] or NULL (requires theta): conf_i for
+ *                   i < k_b, NaN beyond
+ *   workspace       device, >= sv_workspace_bytes(B, K, V), 256-byte aligned
+ * Out-of-range drafted tokens set SV_FLAG_TOKEN_RANGE and are rejected.
+ * NaN logits set SV_FLAG_NONFINITE; that sequence's outputs are unspecified
+ * but in range.
+ * ---------------------------------------------------------------------- */
+sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype,
+                      const void *target_logits, const void *draft_logits,
+                      const int32_t *draft_tokens, const int32_t *draft_len,
+                      const float *temperature, uint64_t seed,
+                      const float *theta, const sv_row_stats_t *draft_stats,
+                      int32_t *out_tokens, int32_t *out_accept_len,
+                      float *out_feature, float *out_conf,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * sv_av_score -- AV scoring of the drafts alone, before the target forward
+ * pass ("Adaptive Verification without a confidence head", sections
+ * "Background", "Scoring the distribution" and "Other features considered":
+ * survival = cumulative product of the confidences).
+ *
+ *   draft_logits    device [B][K][V]
+ *   temperature     device float [B] (0 = greedy: features at tau = 1)
+ *   theta           device float [K+1]
+ *   keep_threshold  > 0: k_b = number of leading drafts whose survival
+ *                   prod_{j<=i} conf_j is >= keep_threshold; <= 0: k_b = K
+ *   out_feature     device float [B][K] (x = -ln E, clamped to [-30, 30])
+ *   out_conf        device float [B][K]
+ *   out_kept_len    device int32 [B] (may be NULL)
+ *   out_draft_stats device [B][K] or NULL: statistics to hand to sv_verify
+ *   workspace       as for sv_verify
+ * ---------------------------------------------------------------------- */
+sv_status_t sv_av_score(int B, int K, int V, sv_dtype_t dtype,
+                        const void *draft_logits, const float *temperature,
+                        const float *theta, float keep_threshold,
+                        float *out_feature, float *out_conf, int32_t *out_kept_len,
+                        sv_row_stats_t *out_draft_stats,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * AV refit ("Adaptive Verification without a confidence head", section
+ * "Fitting the coefficients").
+ *
+ * sv_av_state_bytes(K)  size of the refit state (256-byte aligned buffer):
+ *   status word, round step counter, and fp64 accumulators of the gradient g
+ *   (K+1), the arrow-shaped Hessian (H_ww, H_wb[K], H_bb[K]) and the label
+ *   counts n[K].  Zero it once (sv_av_reset) before the first step.
+ *
+ * sv_av_fit_step -- one decode step of the refit.  Labels are the drafts up
+ *   to and including the first rejection: y = 1 for i < accept_len[b], y = 0
+ *   at i = accept_len[b] if that is < kept_len[b].  The gradient and Hessian
+ *   of the summed log-loss at the current theta are added to the state; on
+ *   the round_len-th step of a round the system H * delta = g is solved over
+ *   the slope and the intercepts that have labels (ridge 1e-9 * trace(H) /
+ *   (K+1) on the diagonal) and theta_j -= n_j / (n_j + damping_c) * delta_j
+ *   (n_omega = all labels of the round); then the accumulators are cleared.
+ *
+ *   theta       device float [K+1], read, and updated at round end
+ *   av_state    device, >= sv_av_state_bytes(K)
+ *   round_len   N >= 1 decode steps per refit
+ *   damping_c   constant of the damping n / (n + c), >= 0
+ *   feature     device float [B][K] (from sv_verify or sv_av_score)
+ *   accept_len  device int32 [B] (from sv_verify)
+ *   kept_len    device int32 [B] or NULL (= K)
+ * ---------------------------------------------------------------------- */
+size_t sv_av_state_bytes(int K);
+sv_status_t sv_av_reset(int K, void *av_state, size_t av_state_bytes, void *stream);
+sv_status_t sv_av_fit_step(int B, int K, float *theta, void *av_state, size_t av_state_bytes,
+                           int round_len, float damping_c,
+                           const float *feature, const int32_t *accept_len,
+                           const int32_t *kept_len, void *stream);
+
+/* ------------------------------------------------------------------------
+ * sv_philox -- the uniform stream itself, for checking: out[b][pos][w] =
+ * word w of Philox4x32-10 with key (seed & 0xffffffff, seed >> 32) and
+ * counter (b, pos, 0, 0) (Salmon, Moraes, Dror, Shaw, "Parallel Random
+ * Numbers: As Easy as 1, 2, 3", SC'11), for b < nb, pos < npos.
+ *   out  device uint32 [nb][npos][4]
+ * ---------------------------------------------------------------------- */
+sv_status_t sv_philox(uint64_t seed, int nb, int npos, uint32_t *out, void *stream);
+
+/* ------------------------------------------------------------------------
+ * sv_status -- synchronise `stream`, read and clear the status word in the
+ * first 4 bytes of `status_holder` (a workspace or an AV state).  Returns
+ * SV_OK, or the most severe error among the bits that were set (TIMEOUT,
+ * NONFINITE, TOKEN_RANGE, BAD_LEN, BAD_TEMP, in that order); the raw bits
+ * go to *flags_out when it is not NULL.  The warning bits SV_FLAG_ZERO_RESIDUAL
+ * and SV_FLAG_FIT_SINGULAR alone map to SV_OK.
+ * ---------------------------------------------------------------------- */
+sv_status_t sv_status(void *status_holder, void *stream, uint32_t *flags_out);
+
+/* ------------------------------------------------------------------------
+ * sv_set_launch_events -- measurement hook.  For the calling host thread,
+ * every later sv_verify / sv_av_score call records `begin_event` on its
+ * stream immediately before launching the row-pass kernel (the streaming
+ * read of all verified rows) and `end_event` immediately after it, so the
+ * caller can time that kernel alone with cudaEventElapsedTime.  Events are
+ * cudaEvent_t passed as void*, owned by the caller; NULL, NULL turns the
+ * hook off.  Nothing else about the calls changes.
+ * ---------------------------------------------------------------------- */
+sv_status_t sv_set_launch_events(void *begin_event, void *end_event);
+
+/* Static description of a status code; never NULL. */
+const char *sv_strerror(sv_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

@@ -72,7 +72,7 @@ def _load():
             lib.orc_av_score.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P,
                                          ctypes.c_double, P, P, P]
             lib.orc_av_score.restype = None
-            lib.orc_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P,
+            lib.orc_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P,
                                        ctypes.c_uint64, P, P, P, P, P, P, P, P]
             lib.orc_verify.restype = None
             lib.orc_av_accumulate.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
@@ -153,13 +153,16 @@ def av_score(draft, temperature, theta, keep_threshold: float = 0.0):
 # --------------------------------------------------------------------------
 # Verification step
 # --------------------------------------------------------------------------
-def verify(target, draft, draft_tokens, temperature, seed: int, draft_len=None, theta=None):
+def verify(target, draft, draft_tokens, temperature, seed: int, draft_len=None, theta=None, seq_ids=None):
     """One verification step.
 
     target [B][K+1][V], draft [B][K][V] (uint16 bf16 bits or float32),
-    draft_tokens [B][K] int32, temperature [B] float32, draft_len [B] or None.
+    draft_tokens [B][K] int32, temperature [B] float32, draft_len [B] or None,
+    seq_ids [B] or None: global sequence indices keying the uniforms.
     Returns dict(tokens [B][K+1], accept_len [B], feature [B][K], conf [B][K],
-    margin [B], ndraws [B], flags [B]).
+    acc_margin [B] (smallest |u - ratio| over the acceptance draws),
+    smp_margin [B] (distance of u R to the chosen CDF step's nearer edge, / R),
+    margin [B] (the smaller of the two), ndraws [B], flags [B]).
     """
     t, code = _logits(target)
     d, code2 = _logits(draft)
@@ -171,12 +174,18 @@ def verify(target, draft, draft_tokens, temperature, seed: int, draft_len=None, 
     tau = np.ascontiguousarray(np.asarray(temperature, dtype=np.float32).reshape(B))
     dl = None if draft_len is None else np.ascontiguousarray(np.asarray(draft_len, dtype=np.int32).reshape(B))
     th = None if theta is None else np.ascontiguousarray(np.asarray(theta, dtype=np.float64).reshape(K + 1))
+    sid = None if seq_ids is None else np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int32).reshape(B))
     out = dict(tokens=np.zeros((B, K + 1), np.int32), accept_len=np.zeros(B, np.int32),
                feature=np.zeros((B, K), np.float64), conf=np.zeros((B, K), np.float64),
-               margin=np.zeros(B, np.float64), ndraws=np.zeros(B, np.int32), flags=np.zeros(B, np.int32))
-    _load().orc_verify(B, K, V, code, _ptr(t), _ptr(d), _ptr(dt), _ptr(dl), _ptr(tau), int(seed) & (2**64 - 1),
+               margins=np.zeros((B, 2), np.float64), ndraws=np.zeros(B, np.int32), flags=np.zeros(B, np.int32))
+    _load().orc_verify(B, K, V, code, _ptr(t), _ptr(d), _ptr(dt), _ptr(dl), _ptr(sid), _ptr(tau),
+                       int(seed) & (2**64 - 1),
                        _ptr(th), _ptr(out["tokens"]), _ptr(out["accept_len"]), _ptr(out["feature"]),
-                       _ptr(out["conf"]), _ptr(out["margin"]), _ptr(out["ndraws"]), _ptr(out["flags"]))
+                       _ptr(out["conf"]), _ptr(out["margins"]), _ptr(out["ndraws"]), _ptr(out["flags"]))
+    out["acc_margin"] = out["margins"][:, 0].copy()
+    out["smp_margin"] = out["margins"][:, 1].copy()
+    out["margin"] = out["margins"].min(axis=1)
+    del out["margins"]
     return out
 
 

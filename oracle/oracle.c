@@ -244,20 +244,23 @@ static int cdf_pick(const double *r, int V, double u, double *margin)
 /* One verification step over B sequences ([SD] "one speculative step").    */
 /*   target      [B][K+1][V]   draft [B][K][V]   draft_tokens [B][K]         */
 /*   draft_len   [B] or NULL (= K): drafts verified for sequence b           */
+/*   seq_ids     [B] or NULL: global sequence index used as the uniforms'    */
+/*               counter (lets a subset of a batch be checked alone)         */
 /*   temperature [B] (0 = greedy)                                            */
 /*   theta       [K+1] or NULL: (omega, beta_0..beta_{K-1}); with theta the  */
 /*               feature and confidence of every verified draft are written  */
 /* Outputs: out_tokens [B][K+1] (-1 padded), out_accept_len [B],             */
 /*   out_feature/out_conf [B][K] (NaN where not verified; may be NULL),      */
-/*   out_margin [B]: smallest margin over the uniforms the sequence consumed */
-/*   (acceptance: |u - ratio|; sampling: distance of u*R to the chosen CDF   */
-/*   step, divided by R); +inf when none was consumed,                       */
+/*   out_margin [B][2]: smallest acceptance margin |u - ratio| over the     */
+/*   acceptance uniforms the sequence consumed, and the sampling margin      */
+/*   (distance of u*R to the nearer edge of the chosen CDF step, divided by  */
+/*   R); +inf when no such uniform was consumed,                             */
 /*   out_ndraws [B]: uniforms consumed, out_flags [B]: ORC_FLAG_* bits.      */
 /* ------------------------------------------------------------------------ */
 void orc_verify(int B, int K, int V, int dtype,
                 const void *target, const void *draft, const int32_t *draft_tokens,
-                const int32_t *draft_len, const float *temperature, uint64_t seed,
-                const double *theta,
+                const int32_t *draft_len, const int32_t *seq_ids, const float *temperature,
+                uint64_t seed, const double *theta,
                 int32_t *out_tokens, int32_t *out_accept_len,
                 double *out_feature, double *out_conf,
                 double *out_margin, int32_t *out_ndraws, int32_t *out_flags)
@@ -271,10 +274,11 @@ void orc_verify(int B, int K, int V, int dtype,
     for (b = 0; b < B; b++) {
         double tau = (double)temperature[b];
         int greedy, k, i, j, a, tok, flags = 0, ndraws = 0;
-        double margin = INFINITY;
+        double margin = INFINITY, smargin = INFINITY;
         const char *trow0 = (const char *)target + (size_t)b * (size_t)(K + 1) * rowb;
         const char *drow0 = (const char *)draft + (size_t)b * (size_t)K * rowb;
         const int32_t *d = draft_tokens + (size_t)b * K;
+        uint32_t sid = seq_ids ? (uint32_t)seq_ids[b] : (uint32_t)b;
 
         if (isnan(tau) || tau < 0.0) { flags |= ORC_FLAG_BAD_TEMP; tau = 0.0; }
         greedy = (tau == 0.0);
@@ -308,7 +312,7 @@ void orc_verify(int B, int K, int V, int dtype,
             if (greedy) {
                 accept = in_range && di == tst[i].argmax;
             } else {
-                double u = orc_uniform(seed, (uint32_t)b, (uint32_t)i, 0u);
+                double u = orc_uniform(seed, sid, (uint32_t)i, 0u);
                 double ratio, mg;
                 ndraws++;
                 if (!in_range) {
@@ -330,7 +334,7 @@ void orc_verify(int B, int K, int V, int dtype,
         if (greedy) {
             tok = tst[a].argmax;
         } else {
-            double u2 = orc_uniform(seed, (uint32_t)b, (uint32_t)a, 1u);
+            double u2 = orc_uniform(seed, sid, (uint32_t)a, 1u);
             double mg, R = 0.0;
             const char *trow = trow0 + (size_t)a * rowb;
             int v;
@@ -350,7 +354,7 @@ void orc_verify(int B, int K, int V, int dtype,
                 for (v = 0; v < V; v++) r[v] = exp(row_logprob(trow, dtype, tau, &tst[a], v));
             }
             tok = cdf_pick(r, V, u2, &mg);
-            if (mg < margin) margin = mg;
+            smargin = mg;
         }
 
         for (j = 0; j <= K; j++) {
@@ -360,7 +364,10 @@ void orc_verify(int B, int K, int V, int dtype,
             out_tokens[(size_t)b * (K + 1) + j] = val;
         }
         out_accept_len[b] = a;
-        if (out_margin) out_margin[b] = margin;
+        if (out_margin) {
+            out_margin[2 * (size_t)b] = margin;
+            out_margin[2 * (size_t)b + 1] = smargin;
+        }
         if (out_ndraws) out_ndraws[b] = ndraws;
         if (out_flags) out_flags[b] = flags;
     }

@@ -1,0 +1,741 @@
+// Row pass: one streaming read of every verified target and draft row.
+//
+// What it computes, per vocabulary row ("Speculative Decoding: Draft, EAGLE,
+// MTP", section "one speculative step": both models return a distribution per
+// drafted position): the raw maximum m, the first argmax, and
+// E = sum_{v != argmax} exp((z_v - m) / tau), so that ln S = log1p(E) and the
+// AV feature logit(q_max) = -ln E ("Adaptive Verification without a confidence
+// head", section "Scoring the distribution").  When the last row of a sequence
+// is done, the same CTA runs the sequence's left-to-right acceptance scan
+// (section "algorithm loop in code" of the cheatsheet) and writes the
+// sampling task for the residual or bonus row.
+//
+// GB300 design: a persistent grid, one CTA per SM, warp-specialised:
+//   warp 8  (producer)  takes work items from a global ticket and streams the
+//                       row bytes with 1-D TMA bulk copies into an 8-stage
+//                       shared-memory ring (16 KB stages, mbarrier complete_tx);
+//   warps 0-7 (math)    read 16-byte vectors from shared memory, keep a
+//                       warp-uniform running max (bf16x2 max + shuffles) and
+//                       a per-lane sum of exp2 terms, exclude exactly one copy
+//                       of the max, and publish one partial per warp and item;
+//   warp 9  (epilogue)  combines the 8 partials, merges row chunks, counts
+//                       finished rows per sequence and runs the scan for the
+//                       sequence whose last row it completed.
+// Every wait is bounded (2 s by default); a time-out sets SV_FLAG_TIMEOUT,
+// drains this CTA's in-flight copies and returns.
+#include <cfloat>
+#include <climits>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+
+namespace {
+
+constexpr int kFlagFirst = 1;
+constexpr int kFlagLast = 2;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kEpilogueWarp = kConsumerWarps + 1;
+constexpr uint32_t kNegInfBf16x2 = 0xff80ff80u;
+constexpr uint32_t kNegInfF32 = 0xff800000u;
+
+struct StageHdr {
+  int item;  // -1: no more work
+  int b;
+  int sidx;   // statistics index inside the sequence: 2j (target j) or 2i+1 (draft i)
+  int chunk;
+  int e0;     // row element index of the first staged element
+  int nvec;   // staged 16-byte vectors
+  int flags;
+  int x0, xn0, x1, xn1;  // elements read with plain loads on the LAST stage
+  float c;               // log2(e) / tau
+  long long row_off;     // element offset of the row inside its tensor
+  int is_target;
+  int pad;
+};
+
+struct PartInfo {
+  int item;
+  int b;
+  int sidx;
+  int chunk;
+  float c;
+  int pad[3];
+};
+
+struct alignas(16) Part {
+  float m;
+  float E;
+  int arg;
+  uint32_t flags;
+};
+
+struct __align__(128) Smem {
+  uint8_t ring[kStages][kStageBytes];
+  StageHdr hdr[kStages];
+  PartInfo pinfo[2];
+  Part part[2][kConsumerWarps];
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t pfull[2];
+  uint64_t pempty[2];
+  int abort_flag;
+};
+
+__device__ __forceinline__ int kept_len_of(const RowPassParams &P, int b) {
+  if (!P.draft_len) return P.K;
+  int k = __ldg(P.draft_len + b);
+  return k < 0 ? 0 : (k > P.K ? P.K : k);
+}
+
+__device__ __forceinline__ float row_scale(const RowPassParams &P, int b) {
+  const float tau = __ldg(P.temperature + b);
+  return tau > 0.f ? kLog2e / tau : kLog2e;  // greedy (and invalid) rows at tau = 1
+}
+
+// Slot -> (is_target, position) for the streaming mode.
+__device__ __forceinline__ void slot_kind(int mode, int slot, int &is_target, int &pos) {
+  if (mode == kVerifyFull) {
+    is_target = !(slot & 1);
+    pos = slot >> 1;
+  } else if (mode == kVerifyTargets) {
+    is_target = 1;
+    pos = slot;
+  } else {
+    is_target = 0;
+    pos = slot;
+  }
+}
+
+__device__ __forceinline__ int rows_needed(const RowPassParams &P, int k) {
+  if (P.mode == kVerifyFull) return 2 * k + 1;
+  if (P.mode == kVerifyTargets) return k + 1;
+  return P.K;
+}
+
+__device__ __forceinline__ Part load_stats_cg(const sv_row_stats_t *p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4 *>(p));
+  Part r;
+  r.m = __int_as_float(v.x);
+  r.E = __int_as_float(v.y);
+  r.arg = v.z;
+  r.flags = (uint32_t)v.w;
+  return r;
+}
+
+__device__ __forceinline__ void store_stats(sv_row_stats_t *p, const Part &s) {
+  int4 v;
+  v.x = __float_as_int(s.m);
+  v.y = __float_as_int(s.E);
+  v.z = s.arg;
+  v.w = (int)s.flags;
+  *reinterpret_cast<int4 *>(p) = v;
+}
+
+// Combine the partial statistics of two disjoint element sets of one row.
+__device__ __forceinline__ Part combine(Part A, Part B, float c) {
+  const bool b_empty = (B.arg == INT_MAX);
+  const bool a_empty = (A.arg == INT_MAX);
+  if (b_empty) {
+    A.flags |= B.flags;
+    if (isnan(B.E)) A.flags |= SV_FLAG_NONFINITE;
+    return A;
+  }
+  if (a_empty) {
+    B.flags |= A.flags;
+    if (isnan(A.E)) B.flags |= SV_FLAG_NONFINITE;
+    return B;
+  }
+  const bool a_wins = (A.m > B.m) || (A.m == B.m && A.arg < B.arg);
+  Part W = a_wins ? A : B;
+  const Part L = a_wins ? B : A;
+  W.E = W.E + (L.E + 1.0f) * ex2_approx((L.m - W.m) * c);
+  W.flags |= L.flags;
+  return W;
+}
+
+__device__ __forceinline__ float logit_at(const void *base, int dtype, long long idx) {
+  if (dtype == SV_BF16) {
+    const uint16_t h = __ldg(reinterpret_cast<const unsigned short *>(base) + idx);
+    return __uint_as_float(((uint32_t)h) << 16);
+  }
+  return __ldg(reinterpret_cast<const float *>(base) + idx);
+}
+
+// ---------------------------------------------------------------------------
+// Math-warp state and the running-max update.
+// ---------------------------------------------------------------------------
+struct WarpState {
+  float M;    // warp-uniform running max of the raw logits
+  float nbh;  // fl(-M * c)
+  float nbl;  // -M * c - nbh, exactly
+  int arg;    // warp-uniform index of the excluded first max
+  float A;    // this lane's sum of 2^(z * c + nbh)
+  uint32_t flags;
+};
+
+__device__ __forceinline__ void state_reset(WarpState &s) {
+  s.M = -INFINITY;
+  s.nbh = 0.f;
+  s.nbl = 0.f;
+  s.arg = INT_MAX;
+  s.A = 0.f;
+  s.flags = 0;
+}
+
+// The warp max rose to wm, attained first at element gidx (already excluded
+// by its owner lane).  Rescale the lane sums to the new max:
+//   A' = (A * 2^nbl_old + [lane 0] * 1) * 2^((M_old - M_new) c - nbl_new)
+// where the "+1" re-admits the previous first max, now an ordinary element.
+__device__ __forceinline__ void state_rise(WarpState &s, float wm, int gidx, float c, int lane) {
+  const float Mold = s.M, nbl_old = s.nbl;
+  s.M = wm;
+  s.nbh = __fmul_rn(-wm, c);
+  s.nbl = fmaf(-wm, c, -s.nbh);
+  const float scale = ex2_approx((Mold - wm) * c - s.nbl);
+  const float fold = fmaf(nbl_old, kLn2, 1.0f);
+  s.A = fmaf(s.A, fold, lane == 0 ? 1.0f : 0.0f) * scale;
+  s.arg = gidx;
+}
+
+template <int kDtype>
+struct Elems;
+
+template <>
+struct Elems<SV_BF16> {
+  static constexpr int kPerVec = 8;
+  __device__ __forceinline__ static float get(const uint4 &w, int k) {
+    const uint32_t x = (k >> 1) == 0 ? w.x : (k >> 1) == 1 ? w.y : (k >> 1) == 2 ? w.z : w.w;
+    return (k & 1) ? bf16hi(x) : bf16lo(x);
+  }
+  __device__ __forceinline__ static void kill(uint4 &w, int k) {
+    const uint32_t mask = (k & 1) ? 0xffff0000u : 0x0000ffffu;
+    const uint32_t ninf = kNegInfBf16x2 & mask;
+    switch (k >> 1) {
+      case 0: w.x = (w.x & ~mask) | ninf; break;
+      case 1: w.y = (w.y & ~mask) | ninf; break;
+      case 2: w.z = (w.z & ~mask) | ninf; break;
+      default: w.w = (w.w & ~mask) | ninf; break;
+    }
+  }
+  __device__ __forceinline__ static uint4 neg_inf() { return make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2); }
+  __device__ __forceinline__ static float vmax(const uint4 (&w)[kVecPerThread]) {
+    uint32_t m0 = bf16x2_max(w[0].x, w[0].y), m1 = bf16x2_max(w[0].z, w[0].w);
+#pragma unroll
+    for (int j = 1; j < kVecPerThread; ++j) {
+      m0 = bf16x2_max(m0, bf16x2_max(w[j].x, w[j].y));
+      m1 = bf16x2_max(m1, bf16x2_max(w[j].z, w[j].w));
+    }
+    const uint32_t m = bf16x2_max(m0, m1);
+    return fmaxf(bf16lo(m), bf16hi(m));
+  }
+};
+
+template <>
+struct Elems<SV_FP32> {
+  static constexpr int kPerVec = 4;
+  __device__ __forceinline__ static float get(const uint4 &w, int k) {
+    const uint32_t x = k == 0 ? w.x : k == 1 ? w.y : k == 2 ? w.z : w.w;
+    return __uint_as_float(x);
+  }
+  __device__ __forceinline__ static void kill(uint4 &w, int k) {
+    switch (k) {
+      case 0: w.x = kNegInfF32; break;
+      case 1: w.y = kNegInfF32; break;
+      case 2: w.z = kNegInfF32; break;
+      default: w.w = kNegInfF32; break;
+    }
+  }
+  __device__ __forceinline__ static uint4 neg_inf() { return make_uint4(kNegInfF32, kNegInfF32, kNegInfF32, kNegInfF32); }
+  __device__ __forceinline__ static float vmax(const uint4 (&w)[kVecPerThread]) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kVecPerThread; ++j)
+      m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(w[j].x), __uint_as_float(w[j].y)),
+                         fmaxf(__uint_as_float(w[j].z), __uint_as_float(w[j].w))));
+    return m;
+  }
+};
+
+// One staged block of vectors: vector j of this lane is vector (tid + j * kConsumers)
+// of the stage, its element k sits at row index e0 + vi * kPerVec + k.
+template <int kDtype>
+__device__ __forceinline__ void consume_vectors(WarpState &s, uint4 (&w)[kVecPerThread], int tid, int lane, int e0,
+                                                float c) {
+  using E = Elems<kDtype>;
+  const float wm = warp_max(E::vmax(w));
+  if (wm > s.M) {  // warp-uniform
+    int cand = INT_MAX;
+#pragma unroll
+    for (int j = kVecPerThread - 1; j >= 0; --j)
+#pragma unroll
+      for (int k = E::kPerVec - 1; k >= 0; --k)
+        if (E::get(w[j], k) == wm) cand = e0 + (tid + j * kConsumers) * E::kPerVec + k;
+    const int gidx = warp_min_i(cand);
+    if (cand == gidx) {
+#pragma unroll
+      for (int j = 0; j < kVecPerThread; ++j)
+#pragma unroll
+        for (int k = 0; k < E::kPerVec; ++k)
+          if (e0 + (tid + j * kConsumers) * E::kPerVec + k == gidx) E::kill(w[j], k);
+    }
+    state_rise(s, wm, gidx, c, lane);
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < kVecPerThread; ++j) {
+    float t[E::kPerVec];
+#pragma unroll
+    for (int k = 0; k < E::kPerVec; ++k) t[k] = ex2_approx(fmaf(E::get(w[j], k), c, s.nbh));
+#pragma unroll
+    for (int h = E::kPerVec / 2; h > 0; h >>= 1)
+#pragma unroll
+      for (int k = 0; k < h; ++k) t[k] += t[k + h];
+    acc += t[0];
+  }
+  s.A += acc;
+}
+
+// Scalar elements (ragged row ends): one value per lane, index idx.
+__device__ __forceinline__ void consume_scalar(WarpState &s, float v, int idx, int lane, float c) {
+  const float wm = warp_max(v);
+  if (wm > s.M) {
+    const int cand = (v == wm) ? idx : INT_MAX;
+    const int gidx = warp_min_i(cand);
+    if (cand == gidx) v = -INFINITY;
+    state_rise(s, wm, gidx, c, lane);
+  }
+  s.A += ex2_approx(fmaf(v, c, s.nbh));
+}
+
+// ---------------------------------------------------------------------------
+// Per-sequence completion (epilogue warp, all 32 lanes).
+// ---------------------------------------------------------------------------
+__device__ void finish_verify(const RowPassParams &P, int b, int lane) {
+  const int K = P.K;
+  const int k = kept_len_of(P, b);
+  const float tau_f = __ldg(P.temperature + b);
+  const bool bad_tau = !(tau_f >= 0.f);
+  const bool greedy = !(tau_f > 0.f);
+  const double invtau = greedy ? 1.0 : 1.0 / (double)tau_f;
+  const size_t rowb = (size_t)P.V;
+  uint32_t flags = 0;
+  if (lane == 0) {
+    if (bad_tau) flags |= SV_FLAG_BAD_TEMP;
+    if (P.draft_len) {
+      const int kr = __ldg(P.draft_len + b);
+      if (kr < 0 || kr > K) flags |= SV_FLAG_BAD_LEN;
+    }
+  }
+  const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
+
+  bool reject = false;
+  int d = -1;
+  if (lane < k) {
+    const int i = lane;
+    const Part T = load_stats_cg(st + 2 * i);
+    const Part D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + i) : load_stats_cg(st + 2 * i + 1);
+    flags |= (T.flags | D.flags) & SV_FLAG_NONFINITE;
+    d = __ldg(P.draft_tokens + (size_t)b * K + i);
+    const bool in_range = d >= 0 && d < P.V;
+    if (!in_range) flags |= SV_FLAG_TOKEN_RANGE;
+    if (greedy) {
+      reject = !(in_range && d == T.arg);
+    } else {
+      const double u = uniform24(P.seed, (uint32_t)b, (uint32_t)i, 0);
+      double ratio = 0.0;
+      if (in_range) {
+        const long long trow = ((long long)b * (K + 1) + i) * (long long)rowb;
+        const long long drow = ((long long)b * K + i) * (long long)rowb;
+        const double zt = (double)logit_at(P.target, P.dtype, trow + d);
+        const double zd = (double)logit_at(P.draft, P.dtype, drow + d);
+        const double lq = (zd - (double)D.m) * invtau - log1p((double)D.E);
+        if (lq == -INFINITY) {
+          ratio = INFINITY;
+        } else {
+          const double lp = (zt - (double)T.m) * invtau - log1p((double)T.E);
+          ratio = exp(lp - lq);
+        }
+      }
+      reject = !(u < ratio);
+    }
+    if (P.out_feature || P.out_conf) {
+      const double E = (double)D.E;
+      double x = E > 0.0 ? -log(E) : 30.0;
+      x = x > 30.0 ? 30.0 : (x < -30.0 ? -30.0 : x);
+      if (P.out_feature) P.out_feature[(size_t)b * K + i] = (float)x;
+      if (P.out_conf) {
+        const double z = (double)__ldg(P.theta) * x + (double)__ldg(P.theta + 1 + i);
+        P.out_conf[(size_t)b * K + i] = (float)(1.0 / (1.0 + exp(-z)));
+      }
+    }
+  } else if (lane < K) {
+    if (P.out_feature) P.out_feature[(size_t)b * K + lane] = __int_as_float(0x7fc00000);
+    if (P.out_conf) P.out_conf[(size_t)b * K + lane] = __int_as_float(0x7fc00000);
+  }
+  const unsigned rej = __ballot_sync(0xffffffffu, reject);
+  const int a = rej ? (__ffs(rej) - 1) : k;
+
+  // Emitted tokens: accepted drafts, the position-a token (written here for
+  // greedy rows, by the sampler otherwise), then -1.
+  const Part Ta = load_stats_cg(st + 2 * a);
+  if (lane <= K) {
+    int32_t v = -1;
+    if (lane < a) v = d;
+    else if (lane == a && greedy) v = (Ta.arg >= 0 && Ta.arg < P.V) ? Ta.arg : 0;
+    P.out_tokens[(size_t)b * (K + 1) + lane] = v;
+  }
+  if (lane == 0) {
+    P.out_accept_len[b] = a;
+    SampleTask t;
+    t.kind = greedy ? kTaskNone : (a < k ? kTaskResidual : kTaskBonus);
+    t.a = a;
+    t.argmax_t = (Ta.arg >= 0 && Ta.arg < P.V) ? Ta.arg : 0;
+    t.c = (float)(kLog2ed * invtau);
+    t.invtau = (float)invtau;
+    const double lnSt = log1p((double)Ta.E);
+    t.nbt = (float)(-((double)Ta.m * (kLog2ed * invtau) + lnSt * kLog2ed));
+    t.k0_hi = 0.f;
+    t.k0_lo = 0.f;
+    if (t.kind == kTaskResidual) {
+      const Part Da = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + a) : load_stats_cg(st + 2 * a + 1);
+      const double k0 = ((double)Ta.m - (double)Da.m) * invtau + lnSt - log1p((double)Da.E);
+      t.k0_hi = (float)k0;
+      t.k0_lo = (float)(k0 - (double)t.k0_hi);
+    }
+    t.u = greedy ? 0.0 : uniform24(P.seed, (uint32_t)b, (uint32_t)a, 1);
+    P.tasks[b] = t;
+  }
+  flags = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && flags) atomicOr(P.status, flags);
+}
+
+__device__ void finish_score(const RowPassParams &P, int b, int lane) {
+  const int K = P.K;
+  const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
+  uint32_t flags = 0;
+  double conf = 1.0;
+  if (lane < K) {
+    const Part D = load_stats_cg(st + 2 * lane + 1);
+    flags |= D.flags & SV_FLAG_NONFINITE;
+    const double E = (double)D.E;
+    double x = E > 0.0 ? -log(E) : 30.0;
+    x = x > 30.0 ? 30.0 : (x < -30.0 ? -30.0 : x);
+    const double z = (double)__ldg(P.theta) * x + (double)__ldg(P.theta + 1 + lane);
+    conf = 1.0 / (1.0 + exp(-z));
+    P.out_feature[(size_t)b * K + lane] = (float)x;
+    P.out_conf[(size_t)b * K + lane] = (float)conf;
+    if (P.out_draft_stats) store_stats(P.out_draft_stats + (size_t)b * K + lane, D);
+  }
+  // survival = cumulative product of the confidences, in position order
+  int kept = K;
+  if (P.keep_threshold > 0.f) {
+    double surv = 1.0;
+    kept = 0;
+    bool stop = false;
+    for (int i = 0; i < K; ++i) {
+      const double ci = __shfl_sync(0xffffffffu, conf, i);
+      if (!stop) {
+        surv *= ci;
+        if (surv >= (double)P.keep_threshold) kept = i + 1;
+        else stop = true;
+      }
+    }
+  }
+  if (lane == 0 && P.out_kept_len) P.out_kept_len[b] = kept;
+  flags = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && flags) atomicOr(P.status, flags);
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+template <int kDtype>
+__global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassParams P) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem &S = *reinterpret_cast<Smem *>(smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u));
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  constexpr int kEsz = kDtype == SV_BF16 ? 2 : 4;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kConsumerWarps);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&S.pfull[s], kConsumerWarps);
+      mbar_init(&S.pempty[s], 1);
+    }
+    S.abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int *abort_flag = &S.abort_flag;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ producer
+    if (lane != 0) return;
+    int s = 0;
+    uint32_t phase = 0;
+    uint32_t nfull[kStages];
+#pragma unroll
+    for (int i = 0; i < kStages; ++i) nfull[i] = 0;
+    int cached_b = -1, cached_k = 0;
+    float cached_c = 1.f;
+    bool ok = true;
+    const int K = P.K;
+    for (;;) {
+      const int item = (int)atomicAdd(P.ticket, 1u);
+      if (item >= P.nitems) break;
+      const int per_seq = P.nslot * P.nch;
+      const int b = item / per_seq;
+      const int rem = item - b * per_seq;
+      const int slot = rem / P.nch;
+      const int chunk = rem - slot * P.nch;
+      if (b != cached_b) {
+        cached_b = b;
+        cached_k = kept_len_of(P, b);
+        cached_c = row_scale(P, b);
+      }
+      int is_target, pos;
+      slot_kind(P.mode, slot, is_target, pos);
+      if (P.mode != kScore) {
+        if (is_target ? (pos > cached_k) : (pos >= cached_k)) continue;
+      }
+      const long long row = is_target ? ((long long)b * (K + 1) + pos) : ((long long)b * K + pos);
+      const long long row_off = row * (long long)P.V;
+      const char *base = reinterpret_cast<const char *>(is_target ? P.target : P.draft);
+      const int e_beg = chunk * P.chunk_elems;
+      const int e_end = min(P.V, e_beg + P.chunk_elems);
+      const uintptr_t a_beg = reinterpret_cast<uintptr_t>(base) + (uintptr_t)(row_off + e_beg) * kEsz;
+      const uintptr_t a_end = reinterpret_cast<uintptr_t>(base) + (uintptr_t)(row_off + e_end) * kEsz;
+      int a0 = e_beg + (int)(((16 - (a_beg & 15)) & 15) / kEsz);
+      int a1 = e_end - (int)((a_end & 15) / kEsz);
+      int x0, xn0, x1, xn1;
+      if (a1 <= a0) {  // no whole aligned vector: every element by plain loads
+        a0 = a1 = e_beg;
+        x0 = e_beg;
+        xn0 = e_end - e_beg;
+        x1 = e_end;
+        xn1 = 0;
+      } else {
+        x0 = e_beg;
+        xn0 = a0 - e_beg;
+        x1 = a1;
+        xn1 = e_end - a1;
+      }
+      const long long mid_bytes = (long long)(a1 - a0) * kEsz;
+      const int nst = mid_bytes > 0 ? (int)((mid_bytes + kStageBytes - 1) / kStageBytes) : 1;
+      const int sidx = is_target ? 2 * pos : 2 * pos + 1;
+      for (int st = 0; st < nst; ++st) {
+        if (!mbar_wait_bounded(&S.empty[s], phase ^ 1u, abort_flag, P.status, P.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        const long long off_b = (long long)st * kStageBytes;
+        const int bytes = mid_bytes > 0 ? (int)min((long long)kStageBytes, mid_bytes - off_b) : 0;
+        StageHdr &h = S.hdr[s];
+        h.item = item;
+        h.b = b;
+        h.sidx = sidx;
+        h.chunk = chunk;
+        h.e0 = a0 + (int)(off_b / kEsz);
+        h.nvec = bytes / 16;
+        h.flags = (st == 0 ? kFlagFirst : 0) | (st == nst - 1 ? kFlagLast : 0);
+        h.x0 = x0;
+        h.xn0 = xn0;
+        h.x1 = x1;
+        h.xn1 = xn1;
+        h.c = cached_c;
+        h.row_off = row_off;
+        h.is_target = is_target;
+        ++nfull[s];
+        if (bytes > 0) {
+          mbar_arrive_expect_tx(&S.full[s], (uint32_t)bytes);
+          bulk_g2s(S.ring[s], base + (row_off + a0) * kEsz + off_b, (uint32_t)bytes, &S.full[s]);
+        } else {
+          mbar_arrive(&S.full[s]);
+        }
+        if (++s == kStages) {
+          s = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+    if (ok && mbar_wait_bounded(&S.empty[s], phase ^ 1u, abort_flag, P.status, P.timeout_ns)) {
+      S.hdr[s].item = -1;
+      ++nfull[s];
+      mbar_arrive(&S.full[s]);
+    } else {
+      // Gave up: wait (bounded) for this CTA's copies still in flight.
+      const uint64_t t0 = global_ns();
+      for (int i = 0; i < kStages; ++i) {
+        if (nfull[i] == 0) continue;
+        while (!mbar_try_wait(&S.full[i], (nfull[i] - 1u) & 1u)) {
+          if (global_ns() - t0 > P.timeout_ns) break;
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp == kEpilogueWarp) {
+    // ------------------------------------------------------------------ epilogue
+    const int K = P.K;
+    for (int it = 0;; ++it) {
+      const int slot = it & 1;
+      if (!mbar_wait_bounded(&S.pfull[slot], (uint32_t)((it >> 1) & 1), abort_flag, P.status, P.timeout_ns)) break;
+      const PartInfo info = S.pinfo[slot];
+      if (info.item < 0) break;
+      Part mine = {-INFINITY, 0.f, INT_MAX, 0u};
+      if (lane < kConsumerWarps) mine = S.part[slot][lane];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.pempty[slot]);
+      int seq_done = 0;
+      // Gather the 8 warp partials into lane 0 in warp order.
+      Part R;
+      R.m = __shfl_sync(0xffffffffu, mine.m, 0);
+      R.E = __shfl_sync(0xffffffffu, mine.E, 0);
+      R.arg = __shfl_sync(0xffffffffu, mine.arg, 0);
+      R.flags = __shfl_sync(0xffffffffu, mine.flags, 0);
+      for (int w = 1; w < kConsumerWarps; ++w) {
+        Part o;
+        o.m = __shfl_sync(0xffffffffu, mine.m, w);
+        o.E = __shfl_sync(0xffffffffu, mine.E, w);
+        o.arg = __shfl_sync(0xffffffffu, mine.arg, w);
+        o.flags = __shfl_sync(0xffffffffu, mine.flags, w);
+        R = combine(R, o, info.c);
+      }
+      if (lane == 0) {
+        const size_t row = (size_t)info.b * (2 * K + 1) + info.sidx;
+        bool row_done = true;
+        if (P.nch > 1) {
+          store_stats(P.chunk_part + row * kMaxChunks + info.chunk, R);
+          __threadfence();
+          const uint32_t old = atomicAdd(P.row_cnt + row, 1u);
+          row_done = (old == (uint32_t)P.nch - 1u);
+          if (row_done) {
+            __threadfence();
+            R = load_stats_cg(P.chunk_part + row * kMaxChunks + 0);
+            for (int c = 1; c < P.nch; ++c) R = combine(R, load_stats_cg(P.chunk_part + row * kMaxChunks + c), info.c);
+          }
+        }
+        if (row_done) {
+          if (R.arg == INT_MAX || !(fabsf(R.m) <= FLT_MAX) || isnan(R.E)) R.flags |= SV_FLAG_NONFINITE;
+          store_stats(P.stats + row, R);
+          __threadfence();
+          const int k = kept_len_of(P, info.b);
+          const uint32_t old = atomicAdd(P.seq_cnt + info.b, 1u);
+          seq_done = (old == (uint32_t)rows_needed(P, k) - 1u);
+          if (seq_done) __threadfence();
+        }
+      }
+      seq_done = __shfl_sync(0xffffffffu, seq_done, 0);
+      if (seq_done) {
+        __threadfence();
+        if (P.mode == kScore) finish_score(P, info.b, lane);
+        else finish_verify(P, info.b, lane);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------------- math warps
+  WarpState st;
+  state_reset(st);
+  int s = 0;
+  uint32_t phase = 0;
+  int it = 0;
+  float c = 1.f;
+  for (;;) {
+    if (!mbar_wait_bounded(&S.full[s], phase, abort_flag, P.status, P.timeout_ns)) break;
+    const StageHdr h = S.hdr[s];
+    if (h.item < 0) {
+      // propagate the end of work to the epilogue warp
+      const int slot = it & 1;
+      if (mbar_wait_bounded(&S.pempty[slot], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag, P.status, P.timeout_ns)) {
+        if (warp == 0 && lane == 0) S.pinfo[slot].item = -1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.pfull[slot]);
+      }
+      break;
+    }
+    if (h.flags & kFlagFirst) {
+      state_reset(st);
+      c = h.c;
+    }
+    uint4 w[kVecPerThread];
+    const uint4 *ring = reinterpret_cast<const uint4 *>(S.ring[s]);
+#pragma unroll
+    for (int j = 0; j < kVecPerThread; ++j) {
+      const int vi = tid + j * kConsumers;
+      w[j] = vi < h.nvec ? ring[vi] : Elems<kDtype>::neg_inf();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[s]);
+    if (h.nvec > 0) consume_vectors<kDtype>(st, w, tid, lane, h.e0, c);
+
+    if (h.flags & kFlagLast) {
+      if (warp == 0) {
+        const int nx = h.xn0 + h.xn1;
+        if (nx > 0) {
+          const int idx = lane < h.xn0 ? h.x0 + lane : h.x1 + (lane - h.xn0);
+          const void *base = h.is_target ? P.target : P.draft;
+          const float v = lane < nx ? logit_at(base, kDtype, h.row_off + idx) : -INFINITY;
+          consume_scalar(st, v, idx, lane, c);
+        }
+      }
+      // warp partial: lane sums in true units, then across the warp
+      const float T = st.A * fmaf(st.nbl, kLn2, 1.0f);
+      const float Ew = warp_sum(T);
+      const int slot = it & 1;
+      if (!mbar_wait_bounded(&S.pempty[slot], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag, P.status, P.timeout_ns)) break;
+      if (lane == 0) {
+        Part pr;
+        pr.m = st.M;
+        pr.E = Ew;
+        pr.arg = st.arg;
+        pr.flags = st.flags;
+        S.part[slot][warp] = pr;
+        if (warp == 0) {
+          PartInfo pi;
+          pi.item = h.item;
+          pi.b = h.b;
+          pi.sidx = h.sidx;
+          pi.chunk = h.chunk;
+          pi.c = c;
+          S.pinfo[slot] = pi;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.pfull[slot]);
+      ++it;
+    }
+    if (++s == kStages) {
+      s = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+}  // namespace
+
+size_t rowpass_smem_bytes() { return sizeof(Smem) + 128; }
+
+cudaError_t launch_rowpass(const RowPassParams &P, int grid, cudaStream_t stream) {
+  const size_t smem = rowpass_smem_bytes();
+  if (P.dtype == SV_BF16) {
+    cudaFuncSetAttribute(rowpass_kernel<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    rowpass_kernel<SV_BF16><<<grid, kRowThreads, smem, stream>>>(P);
+  } else {
+    cudaFuncSetAttribute(rowpass_kernel<SV_FP32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    rowpass_kernel<SV_FP32><<<grid, kRowThreads, smem, stream>>>(P);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -1,0 +1,168 @@
+// Internal definitions shared by the host API and the kernels: launch
+// parameters, the per-sequence sampling task, and the workspace layout.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "specverify.h"
+
+namespace sv {
+
+// ---- row pass geometry -----------------------------------------------------
+constexpr int kStageBytes = 32768;                 // one TMA bulk copy
+constexpr int kStages = 6;                         // ring depth (192 KB in flight per SM)
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;    // 512 math threads
+constexpr int kRowThreads = kConsumers + 64;       // + producer warp + epilogue warp
+constexpr int kVecPerStage = kStageBytes / 16;     // 2048 16-byte vectors
+constexpr int kVecPerThread = kVecPerStage / kConsumers;  // 4
+constexpr int kMaxChunks = 16;                     // chunks a row may be split into
+constexpr int kChunkAlignElems = 512;              // chunk starts stay 16-byte aligned within a row
+
+// Row pass modes: which rows of a sequence are streamed.
+enum RowMode : int {
+  kVerifyFull = 0,     // slots t0 d0 t1 d1 ... tK (target and draft rows)
+  kVerifyTargets = 1,  // slots t0 .. tK (draft statistics supplied by the caller)
+  kScore = 2           // slots d0 .. d{K-1} (AV scoring only)
+};
+
+// ---- sampling ----------------------------------------------------------------
+constexpr int kSampleThreads = 256;
+constexpr int kSampleWarps = kSampleThreads / 32;
+constexpr int kSubChunk = 32 * 8;                  // 256 elements per partial sum (one warp, 8 per lane)
+constexpr int kSampleUnroll = 4;                   // sub-chunks a warp loads before reducing
+
+enum TaskKind : int { kTaskNone = 0, kTaskResidual = 1, kTaskBonus = 2 };
+
+// Everything the sampler needs for sequence b, written by the acceptance scan.
+//   p_v  proportional to 2^(z_t[v] * c + nbt)
+//   delta_v = ln q_v - ln p_v = (z_d[v] - z_t[v]) * invtau + (k0_hi + k0_lo)
+//   residual weight r_v = p_v * (1 - e^delta_v) where delta_v < 0, else 0
+struct SampleTask {
+  int32_t kind;
+  int32_t a;       // position whose row is sampled
+  float c;         // log2(e) / tau
+  float invtau;    // 1 / tau
+  float nbt;       // -(m_t * c + ln S_t * log2 e), rounded
+  float k0_hi;     // (m_t - m_d) / tau + ln S_t - ln S_d, split in two floats
+  float k0_lo;
+  int32_t argmax_t;  // fallback token
+  double u;        // U(seed, b, a, 1)
+};
+
+struct RowPassParams {
+  const void *target;
+  const void *draft;
+  const int32_t *draft_tokens;
+  const int32_t *draft_len;
+  const float *temperature;
+  const float *theta;
+  const sv_row_stats_t *draft_stats_in;
+  int B, K, V, esz, dtype;
+  int mode;
+  int nslot;        // row slots per sequence in this mode
+  int nch;          // chunks per row
+  int chunk_elems;  // elements per chunk (multiple of kChunkAlignElems unless nch == 1)
+  int nitems;       // B * nslot * nch
+  uint64_t seed;
+  float keep_threshold;
+  // outputs
+  int32_t *out_tokens;
+  int32_t *out_accept_len;
+  float *out_feature;
+  float *out_conf;
+  int32_t *out_kept_len;
+  sv_row_stats_t *out_draft_stats;
+  // workspace
+  uint32_t *status;
+  uint32_t *ticket;
+  uint32_t *row_cnt;       // [B][2K+1]
+  uint32_t *seq_cnt;       // [B]
+  sv_row_stats_t *stats;   // [B][2K+1]: target j at 2j, draft i at 2i+1
+  sv_row_stats_t *chunk_part;  // [B][2K+1][kMaxChunks]
+  SampleTask *tasks;       // [B]
+  unsigned long long timeout_ns;
+};
+
+struct SampleParams {
+  const void *target;
+  const void *draft;
+  int B, K, V, esz, dtype;
+  int nsub;       // sub-chunks per row
+  int per_cta;    // CTAs per sequence
+  int32_t *out_tokens;
+  uint32_t *status;
+  uint32_t *smp_cnt;  // [B]
+  float *subsum;      // [B][nsub]
+  const SampleTask *tasks;
+};
+
+// ---- workspace layout --------------------------------------------------------
+struct WsLayout {
+  size_t counters_off, counters_bytes;  // zeroed by every call
+  size_t ticket_off, row_cnt_off, seq_cnt_off, smp_cnt_off;
+  size_t stats_off, chunk_off, task_off, subsum_off;
+  size_t total;
+};
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int B, int K, int V) {
+  WsLayout L{};
+  const size_t nrow = (size_t)B * (size_t)(2 * K + 1);
+  const size_t nsub = ((size_t)V + kSubChunk - 1) / kSubChunk;
+  size_t off = 256;  // status word and spare header
+  L.counters_off = off;
+  L.ticket_off = off;
+  off += 16;
+  L.row_cnt_off = off;
+  off += nrow * 4;
+  L.seq_cnt_off = off;
+  off += (size_t)B * 4;
+  L.smp_cnt_off = off;
+  off += (size_t)B * 4;
+  off = align_up(off, 256);
+  L.counters_bytes = off - L.counters_off;
+  L.stats_off = off;
+  off = align_up(off + nrow * sizeof(sv_row_stats_t), 256);
+  L.chunk_off = off;
+  off = align_up(off + nrow * kMaxChunks * sizeof(sv_row_stats_t), 256);
+  L.task_off = off;
+  off = align_up(off + (size_t)B * sizeof(SampleTask), 256);
+  L.subsum_off = off;
+  off = align_up(off + (size_t)B * nsub * sizeof(float), 256);
+  L.total = off;
+  return L;
+}
+
+// ---- AV refit state ------------------------------------------------------------
+constexpr int kFitSeqPerCta = 128;
+constexpr int kFitMaxCtas = 64;
+constexpr int kFitQ = 6;  // per position: g_w part, H_ww part, g_b, H_wb, H_bb, n
+
+struct AvStateHeader {
+  uint32_t status;
+  uint32_t step;       // decode steps accumulated in the current round
+  uint32_t cta_done;   // arrivals of the current launch (self-resetting)
+  uint32_t K;
+};
+
+// Layout inside the AV state buffer (all doubles):
+//   [header 256 B] [acc: g (K+1), Hww (1), Hwb (K), Hbb (K), n (K)]
+//   [partials: kFitMaxCtas x SV_MAX_K x kFitQ]
+constexpr size_t kAvAccOff = 256;
+constexpr size_t kAvAccDoubles = 4 * SV_MAX_K + 2;
+constexpr size_t kAvPartOff = align_up(kAvAccOff + kAvAccDoubles * 8, 256);
+
+struct FitParams {
+  int B, K, round_len;
+  float damping_c;
+  float *theta;
+  const float *feature;
+  const int32_t *accept_len;
+  const int32_t *kept_len;
+  unsigned char *state;
+};
+
+}  // namespace sv

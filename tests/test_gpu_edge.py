@@ -1,0 +1,174 @@
+"""GPU edge cases: empty and ragged canvases, unaligned and tiny vocabularies,
+split rows, error flags, workspace reuse, determinism, invariances."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_rel, compare, gpu_verify, oracle_verify
+from speculative_decoding_verification_03_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    binding.build()
+    oracle.build()
+
+
+def _rand_workload(B, K, V, dtype=torch.float32, seed=0, noise=0.7, scale=2.0, tau=1.0):
+    g = torch.Generator().manual_seed(seed)
+    z = torch.randn((B, K + 1, V), generator=g) * scale
+    d = z[:, :K] + torch.randn((B, K, V), generator=g) * noise
+    t, dd = z.to(dtype), d.to(dtype)
+    probs = torch.softmax(dd.float() / tau, -1).reshape(-1, V) if K > 0 else None
+    toks = (torch.multinomial(probs, 1, generator=g).view(B, K) if K > 0 else torch.zeros((B, 0), dtype=torch.int64))
+    return synth.Workload("rand", B, K, V, dtype, t.contiguous(), dd.contiguous(), toks.to(torch.int32),
+                          torch.full((B,), float(tau)))
+
+
+def _check(w, seed, theta=None, draft_len=None):
+    g = gpu_verify(w, seed, theta=theta, draft_len=draft_len)
+    assert g["rc"] == 0, g["flags"]
+    r = oracle_verify(w, seed, theta=theta, draft_len=draft_len)
+    compare(g, r)
+    if theta is not None:
+        assert_rel(g["conf"], r["conf"], what="conf")
+    return g, r
+
+
+def test_k0_is_plain_sampling():
+    w = _rand_workload(16, 0, 100, seed=1)
+    g, r = _check(w, 3)
+    assert np.all(g["accept_len"] == 0)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ragged_draft_len(dtype):
+    w = _rand_workload(64, 6, 500, dtype=dtype, seed=2)
+    dl = np.random.default_rng(0).integers(0, 7, 64).astype(np.int32)
+    dl[:3] = [0, 6, 1]
+    th = np.concatenate([[0.5], np.linspace(0.5, -0.5, 6)])
+    g, r = _check(w, 4, theta=th, draft_len=dl)
+    assert np.all(g["accept_len"] <= dl)
+    assert np.isnan(g["conf"][0]).all()  # nothing verified: no score
+
+
+@pytest.mark.parametrize("V,dtype", [(1001, torch.bfloat16), (37, torch.float32), (1, torch.float32),
+                                     (2, torch.bfloat16), (7, torch.bfloat16), (8195, torch.float32),
+                                     (32001, torch.bfloat16)])
+def test_unaligned_and_tiny_vocab(V, dtype):
+    w = _rand_workload(24, 3, V, dtype=dtype, seed=V)
+    th = np.array([0.6, 0.4, 0.1, -0.3])
+    g, r = _check(w, V, theta=th)
+    if V == 1:
+        assert np.all(g["accept_len"] == 3) and np.all(g["tokens"] == 0)
+
+
+@pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 128256), (torch.float32, 300007)])
+def test_split_rows(dtype, V):
+    # few rows with a long vocabulary: each row is split into chunks merged on the device
+    w = _rand_workload(2, 1, V, dtype=dtype, seed=5, scale=3.0, noise=1.0)
+    th = np.array([0.5, 0.3])
+    _check(w, 11, theta=th)
+
+
+def test_draft_equal_target_accepts_all():
+    w = _rand_workload(128, 4, 256, seed=6, noise=0.0)
+    w.draft = w.target[:, :4].contiguous()
+    p = torch.softmax(w.draft, -1).reshape(-1, 256)
+    w.draft_tokens = torch.multinomial(p, 1, generator=torch.Generator().manual_seed(1)).view(128, 4).to(torch.int32)
+    g, r = _check(w, 1)
+    assert np.all(g["accept_len"] == 4)
+
+
+def test_mixed_temperatures_and_greedy_rows():
+    w = _rand_workload(96, 5, 3000, dtype=torch.bfloat16, seed=7)
+    tau = np.random.default_rng(1).uniform(0.3, 1.2, 96).astype(np.float32)
+    tau[::7] = 0.0
+    w.temperature = torch.from_numpy(tau)
+    th = np.concatenate([[0.5], np.zeros(5)])
+    _check(w, 8, theta=th)
+
+
+def test_temperature_scaling_invariance():
+    w = _rand_workload(64, 4, 777, dtype=torch.bfloat16, seed=8, tau=0.7)
+    g1 = gpu_verify(w, 5)
+    w2 = synth.Workload("s", w.B, w.K, w.V, w.dtype, w.target * 2, w.draft * 2, w.draft_tokens, w.temperature * 2)
+    g2 = gpu_verify(w2, 5)
+    assert np.array_equal(g1["tokens"], g2["tokens"]) and np.array_equal(g1["accept_len"], g2["accept_len"])
+
+
+def test_determinism_and_workspace_reuse():
+    w = synth.c2(seed=3, device="cuda")
+    th = np.concatenate([[1.0], np.zeros(w.K)])
+    ws = binding.workspace(256, 5, 128256)  # larger than needed, reused
+    g1 = gpu_verify(w, 1, theta=th, ws=ws)
+    g2 = gpu_verify(w, 1, theta=th, ws=ws)
+    for k in ("tokens", "accept_len", "conf", "feature"):
+        assert np.array_equal(g1[k], g2[k], equal_nan=True), k
+    small = _rand_workload(8, 2, 64, seed=9)
+    gs = gpu_verify(small, 2, ws=ws)
+    rs = oracle_verify(small, 2)
+    compare(gs, rs)
+    g3 = gpu_verify(w, 1, theta=th, ws=ws)
+    assert np.array_equal(g1["tokens"], g3["tokens"])
+
+
+def test_error_flags_are_reported_not_trapped():
+    w = _rand_workload(6, 3, 200, seed=10)
+    toks = w.draft_tokens.clone()
+    toks[1, 0] = 200 + 5
+    toks[2, 1] = -3
+    w.draft_tokens = toks
+    g = gpu_verify(w, 1)
+    assert g["rc"] == 5, g
+    assert g["flags"] & binding.FLAG_TOKEN_RANGE
+    r = oracle_verify(w, 1)
+    compare(g, r)
+    assert g["accept_len"][1] == 0
+    # status is cleared by reading it
+    rc, flags = binding.status(g["ws"])
+    assert rc == 0 and flags == 0
+
+    w2 = _rand_workload(4, 2, 64, seed=11)
+    w2.target[2, 1, 7] = float("nan")
+    g2 = gpu_verify(w2, 1)
+    assert g2["rc"] == 4 and g2["flags"] & binding.FLAG_NONFINITE
+    ok = np.array([0, 1, 3])
+    r2 = oracle_verify(w2, 1)
+    assert np.array_equal(g2["tokens"][ok], r2["tokens"][ok])
+    assert np.all((g2["tokens"] >= -1) & (g2["tokens"] < 64))
+
+    w3 = _rand_workload(4, 2, 64, seed=12)
+    g3 = gpu_verify(w3, 1, draft_len=np.array([2, 5, -1, 1], np.int32))
+    assert g3["rc"] == 8 and g3["flags"] & binding.FLAG_BAD_LEN
+    r3 = oracle_verify(w3, 1, draft_len=np.array([2, 5, -1, 1], np.int32))
+    assert np.array_equal(g3["tokens"], r3["tokens"])
+
+    w4 = _rand_workload(4, 2, 64, seed=13)
+    w4.temperature = torch.tensor([1.0, -0.5, 1.0, float("nan")])
+    g4 = gpu_verify(w4, 1)
+    assert g4["rc"] == 9 and g4["flags"] & binding.FLAG_BAD_TEMP
+    r4 = oracle_verify(w4, 1)
+    assert np.array_equal(g4["tokens"], r4["tokens"])
+
+
+def test_host_checks_with_gpu_present():
+    dev = torch.device("cuda")
+    t = torch.zeros((2, 3, 64), device=dev)
+    d = torch.zeros((2, 2, 64), device=dev)
+    toks = torch.zeros((2, 2), dtype=torch.int32, device=dev)
+    tau = torch.ones(2, device=dev)
+    with pytest.raises(binding.SVError) as e:
+        binding.verify(t, d, toks, tau, 0, ws=torch.empty(16, dtype=torch.uint8, device=dev))
+    assert e.value.code == 7
+    out = binding.verify(t, d, toks, tau, 0)
+    L = binding.lib()
+    import ctypes
+    rc = L.sv_verify(2, 2, 64, 1, ctypes.c_void_p(t.data_ptr() + 2), ctypes.c_void_p(d.data_ptr()),
+                     ctypes.c_void_p(toks.data_ptr()), None, ctypes.c_void_p(tau.data_ptr()), 0, None, None,
+                     ctypes.c_void_p(out["tokens"].data_ptr()), ctypes.c_void_p(out["accept_len"].data_ptr()),
+                     None, None, ctypes.c_void_p(out["ws"].data_ptr()), out["ws"].numel(), None)
+    assert rc == 1  # logits not aligned to their element size
