@@ -230,6 +230,44 @@ sv_status_t sv_philox(uint64_t seed, int nb, int npos, uint32_t *out, void *stre
 sv_status_t sv_status(void *status_holder, void *stream, uint32_t *flags_out);
 
 /* ------------------------------------------------------------------------
+ * sv_verify_noalloc -- sv_verify for callers that cannot allocate device
+ * memory.  (This entry point has no counterpart in the pages; it is a
+ * deployment convenience.)  Some callers hold no device allocator of their
+ * own: a plain C host that only receives pointers to tensors owned by
+ * another framework, or a serving runtime that reserves all device memory
+ * up front for its KV-cache pool and forbids later cudaMalloc (which can
+ * fail under a full pool and synchronises the device).  This entry point
+ * takes the same arguments as sv_verify minus the workspace and uses a
+ * scratch array of SV_NOALLOC_SCRATCH_BYTES compiled into the library
+ * instead; every GPU that loads the library holds that array until the
+ * process exits.  It allocates nothing: no cudaMalloc, no cudaFree.
+ *  - Shapes needing more than SV_NOALLOC_SCRATCH_BYTES of scratch
+ *    (sv_workspace_bytes(B, K, V) > SV_NOALLOC_SCRATCH_BYTES) are rejected
+ *    with SV_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (once per device); make that first call before
+ *    any stream capture.
+ *  - All calls share the one array, and the array keeps the last call's
+ *    contents (each call clears what must start at zero).  Calls that
+ *    overlap on the GPU -- on different streams, or from different host
+ *    threads without ordering -- race on it: order them.
+ *  - sv_status(sv_noalloc_status_holder(), stream, ...) reads its status
+ *    word.
+ * ---------------------------------------------------------------------- */
+#define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
+sv_status_t sv_verify_noalloc(int B, int K, int V, sv_dtype_t dtype,
+                              const void *target_logits, const void *draft_logits,
+                              const int32_t *draft_tokens, const int32_t *draft_len,
+                              const float *temperature, uint64_t seed,
+                              const float *theta, const sv_row_stats_t *draft_stats,
+                              int32_t *out_tokens, int32_t *out_accept_len,
+                              float *out_feature, float *out_conf, void *stream);
+
+/* Device address of the scratch array's status word on the current device
+ * (NULL before the first sv_verify_noalloc call there, or on error). */
+void *sv_noalloc_status_holder(void);
+
+/* ------------------------------------------------------------------------
  * sv_set_launch_events -- measurement hook.  For the calling host thread,
  * every later sv_verify / sv_av_score call records `begin_event` on its
  * stream immediately before launching the row-pass kernel (the streaming

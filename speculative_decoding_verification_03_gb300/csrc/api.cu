@@ -311,6 +311,58 @@ sv_status_t sv_set_launch_events(void *begin_event, void *end_event) {
   return SV_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Scratch for sv_verify_noalloc: a file-scope device array, so the entry
+// point needs no allocation.  Host code cannot use the symbol as a device
+// address; noalloc_scratch() looks the address up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64];
+
+sv_status_t noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return SV_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SV_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sv_status_t sv_verify_noalloc(int B, int K, int V, sv_dtype_t dtype, const void *target_logits,
+                              const void *draft_logits, const int32_t *draft_tokens, const int32_t *draft_len,
+                              const float *temperature, uint64_t seed, const float *theta,
+                              const sv_row_stats_t *draft_stats, int32_t *out_tokens, int32_t *out_accept_len,
+                              float *out_feature, float *out_conf, void *stream) {
+  if (!shape_ok(B, K, V)) return SV_ERR_INVALID;
+  if (sv_workspace_bytes(B, K, V) > (size_t)SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  const sv_status_t st = noalloc_scratch(&scratch);
+  if (st != SV_OK) return st;
+  return sv_verify(B, K, V, dtype, target_logits, draft_logits, draft_tokens, draft_len, temperature, seed, theta,
+                   draft_stats, out_tokens, out_accept_len, out_feature, out_conf, scratch,
+                   (size_t)SV_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+void *sv_noalloc_status_holder(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  return g_noalloc_ptr[dev];
+}
+
 const char *sv_strerror(sv_status_t s) {
   switch (s) {
     case SV_OK: return "ok";
