@@ -54,7 +54,7 @@ def _peak():
 def _kernel_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_03_gb300", "csrc")
-    for fn in ("rowpass.cu", "sv_device.cuh", "sv_internal.h"):
+    for fn in ("rowpass.cu", "sv_device.cuh", "sv_internal.h", "sample_common.cuh"):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -135,22 +135,25 @@ def _dist():
 
 
 def _bytes_per_step(wl, K, V, esz, kept, accept):
-    """Algorithmic bytes of one step.  Returns (bytes of the row-pass launch
-    that the launch events bracket, all bytes of the step).  The step reads
-    every verified target row (k_b + 1) and draft row (k_b) once, re-reads
-    the residual or bonus target row (+ the draft row when rejected), and
-    moves 4 B (3K + 4) of small per-sequence inputs and outputs.  On the
-    AV-truncated canvas the scoring call reads all K draft rows, and the
-    verify row pass (the bracketed one) then reads only the k_b + 1 target
-    rows."""
+    """Algorithmic bytes of one step.  Returns (bytes of the verify row-pass
+    launch that the launch events bracket, all bytes of the step).  The step
+    reads every verified target row (k_b + 1) and draft row (k_b) once,
+    re-reads the residual or bonus target row (+ the draft row when
+    rejected), and moves 4 B (3K + 4) of small per-sequence inputs and
+    outputs.  On the AV-truncated canvas the scoring call reads all K draft
+    rows, and the verify row pass then reads only the k_b + 1 target rows
+    (plus the second pass)."""
     B = kept.size
     second = int(B + (accept < kept).sum()) * V * esz
     small = 4 * B * (3 * K + 4)
     if wl == "c5":
-        bracketed = int((kept + 1).sum()) * V * esz
-        first = bracketed + B * K * V * esz
+        verify_first = int((kept + 1).sum()) * V * esz
+        first = verify_first + B * K * V * esz
     else:
-        bracketed = first = int((2 * kept + 1).sum()) * V * esz
+        verify_first = first = int((2 * kept + 1).sum()) * V * esz
+    # the bracketed verify row pass also samples (second-pass rows) when the
+    # rows are 16-byte aligned, as on every workload here
+    bracketed = verify_first + second + small
     return bracketed, first + second + small
 
 

@@ -40,7 +40,7 @@ def build(force: bool = False, nvcc: str = "nvcc") -> str:
     """Compile the CUDA sources for sm_103a into libspecverify.so (in-tree)."""
     csrc = os.path.join(_HERE, "csrc")
     srcs = [os.path.join(csrc, s) for s in _SOURCES]
-    deps = srcs + [os.path.join(csrc, h) for h in ("sv_device.cuh", "sv_internal.h")] + \
+    deps = srcs + [os.path.join(csrc, h) for h in ("sv_device.cuh", "sv_internal.h", "sample_common.cuh")] + \
         [os.path.join(_ROOT, "include", "specverify.h")]
     if not force and os.path.exists(LIB_PATH) and \
             os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(d) for d in deps):

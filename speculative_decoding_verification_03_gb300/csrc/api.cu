@@ -160,13 +160,6 @@ sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype, const void *target_
   fill_ws(P, workspace, L);
 
   unsigned char *w = static_cast<unsigned char *>(workspace);
-  // status word (offset 0) and the per-call counters, in one clear
-  cudaError_t e = cudaMemsetAsync(w, 0, L.counters_off + L.counters_bytes, st);
-  if (e != cudaSuccess) return SV_ERR_CUDA;
-  const int grid = P.nitems < sms ? P.nitems : sms;
-  e = rowpass_timed(P, grid, st);
-  if (e != cudaSuccess) return SV_ERR_CUDA;
-
   SampleParams S;
   std::memset(&S, 0, sizeof S);
   S.target = target_logits;
@@ -177,16 +170,43 @@ sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype, const void *target_
   S.esz = esz;
   S.dtype = dtype;
   S.nsub = (V + kSubChunk - 1) / kSubChunk;
-  int per = (4 * sms + B - 1) / B;
-  if (per > S.nsub) per = S.nsub;
-  if (per < 1) per = 1;
-  S.per_cta = per;
   S.out_tokens = out_tokens;
   S.status = P.status;
   S.smp_cnt = reinterpret_cast<uint32_t *>(w + L.smp_cnt_off);
   S.subsum = reinterpret_cast<float *>(w + L.subsum_off);
   S.tasks = P.tasks;
-  e = launch_sample(S, B * per, st);
+
+  // Sampling runs inside the row pass (residual and bonus rows re-read while
+  // L2-resident) when every row starts on a 16-byte boundary; otherwise a
+  // separate sampler kernel follows the row pass.
+  P.nstatic = P.nitems;
+  P.fused = ((size_t)V * esz) % 16 == 0 && aligned(target_logits, 16) && (!draft_logits || aligned(draft_logits, 16));
+  if (P.fused) {
+    int sp = (S.nsub + 127) / 128;
+    sp = sp < 1 ? 1 : (sp > kMaxSampleParts ? kMaxSampleParts : sp);
+    P.sp = sp;
+    P.spc = (S.nsub + sp - 1) / sp;
+    P.ndyn = B * sp;
+    P.dq = reinterpret_cast<int *>(w + L.dq_off);
+    P.dq_tail = P.ticket + 1;
+    P.dq_head = P.ticket + 2;
+    P.smp = S;
+  }
+
+  // status word (offset 0) and the per-call counters, in one clear
+  cudaError_t e = cudaMemsetAsync(w, 0, L.counters_off + L.counters_bytes, st);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  const long long tickets = (long long)P.nitems + (P.fused ? P.ndyn : 0);
+  const int grid = tickets < sms ? (int)tickets : sms;
+  e = rowpass_timed(P, grid, st);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  if (P.fused) return SV_OK;
+
+  const long long groups = (long long)B * ((S.nsub + kSampleUnroll - 1) / kSampleUnroll);
+  long long sgrid = (long long)sms * kSampleCtasPerSm;
+  const long long need = (groups + kSampleWarps - 1) / kSampleWarps;
+  if (need < sgrid) sgrid = need;
+  e = launch_sample(S, (int)sgrid, st);
   return cuda_status(e);
 }
 
@@ -228,6 +248,7 @@ sv_status_t sv_av_score(int B, int K, int V, sv_dtype_t dtype, const void *draft
   choose_chunks(B * K, V, sms, P.nch, P.chunk_elems);
   P.nitems = B * K * P.nch;
   P.keep_threshold = keep_threshold;
+  P.nstatic = P.nitems;
   P.out_feature = out_feature;
   P.out_conf = out_conf;
   P.out_kept_len = out_kept_len;
@@ -272,7 +293,7 @@ sv_status_t sv_av_fit_step(int B, int K, float *theta, void *av_state, size_t av
   F.accept_len = accept_len;
   F.kept_len = kept_len;
   F.state = static_cast<unsigned char *>(av_state);
-  int grid = (B + kFitSeqPerCta - 1) / kFitSeqPerCta;
+  int grid = (B + kFitSeqPerCta - 1) / kFitSeqPerCta;  // about 64 sequences per CTA
   if (grid < 1) grid = 1;
   if (grid > kFitMaxCtas) grid = kFitMaxCtas;
   return cuda_status(launch_avfit(F, grid, static_cast<cudaStream_t>(stream)));

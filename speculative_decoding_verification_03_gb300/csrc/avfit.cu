@@ -15,10 +15,11 @@
 //   delta_w = (g_w - sum_i H_wb[i] g_b[i] / d_i) / (H_ww - sum_i H_wb[i]^2 / d_i)
 //   delta_b[i] = (g_b[i] - H_wb[i] delta_w) / d_i,  d_i = H_bb[i] (+ ridge)
 // Layout: grid of G CTAs over the sequences; warp i of a CTA owns position i;
-// lanes stride over the CTA's sequences and accumulate six fp64 sums; CTA
-// partials go to the state buffer; the last CTA (atomic counter) adds them in
-// CTA order (deterministic), updates the round accumulators and, at the end
-// of the round, solves and writes theta.
+// lanes stride over the CTA's sequences and accumulate six sums; CTA
+// partials go to the state buffer; in the last CTA (atomic counter) warp 0
+// adds them in CTA order (deterministic), lane i owning position i, updates
+// the fp64 round accumulators and, at the end of the round, solves with warp
+// reductions for the Schur terms and writes theta.
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -32,15 +33,18 @@ __global__ void avfit_kernel(const FitParams P) {
   const int G = gridDim.x;
   AvStateHeader *hdr = reinterpret_cast<AvStateHeader *>(P.state);
   double *acc = reinterpret_cast<double *>(P.state + kAvAccOff);
-  double *parts = reinterpret_cast<double *>(P.state + kAvPartOff);
+  float *parts = reinterpret_cast<float *>(P.state + kAvPartOff);
   __shared__ int s_last;
 
+  // Per-label terms in fp32 (fp64 issues at a small fraction of the fp32 rate
+  // on this GPU); per-CTA sums of at most a few hundred labels stay well
+  // inside fp32 precision.  The round accumulators and the solve are fp64.
   const int per = (P.B + G - 1) / G;
   const int b0 = blockIdx.x * per, b1 = min(P.B, b0 + per);
   const int i = warp;
-  double q[kFitQ] = {0, 0, 0, 0, 0, 0};
   if (i < K) {
-    const double om = (double)__ldg(P.theta), be = (double)__ldg(P.theta + 1 + i);
+    float q[kFitQ] = {0, 0, 0, 0, 0, 0};
+    const float om = __ldg(P.theta), be = __ldg(P.theta + 1 + i);
     for (int b = b0 + lane; b < b1; b += 32) {
       int k = P.kept_len ? __ldg(P.kept_len + b) : K;
       k = k < 0 ? 0 : (k > K ? K : k);
@@ -48,22 +52,25 @@ __global__ void avfit_kernel(const FitParams P) {
       a = a < 0 ? 0 : (a > k ? k : a);
       const bool labelled = (i < a) || (i == a && a < k);
       if (!labelled) continue;
-      const double y = i < a ? 1.0 : 0.0;
-      const double x = (double)__ldg(P.feature + (size_t)b * K + i);
-      const double s = 1.0 / (1.0 + exp(-(om * x + be)));
-      const double w = s * (1.0 - s);
-      q[0] += (s - y) * x;
-      q[1] += w * x * x;
-      q[2] += (s - y);
-      q[3] += w * x;
+      const float x = __ldg(P.feature + (size_t)b * K + i);
+      const float sg = 1.0f / (1.0f + expf(-fmaf(om, x, be)));
+      const float y = i < a ? 1.0f : 0.0f;
+      const float w = sg * (1.0f - sg);
+      q[0] = fmaf(sg - y, x, q[0]);
+      q[1] = fmaf(w * x, x, q[1]);
+      q[2] += sg - y;
+      q[3] = fmaf(w, x, q[3]);
       q[4] += w;
-      q[5] += 1.0;
+      q[5] += 1.0f;
     }
 #pragma unroll
-    for (int j = 0; j < kFitQ; ++j) q[j] = warp_sum_d(q[j]);
-    if (lane == 0) {
+    for (int j = 0; j < kFitQ; ++j) q[j] = warp_sum(q[j]);
+    if (lane < kFitQ) {
+      float v = q[0];
 #pragma unroll
-      for (int j = 0; j < kFitQ; ++j) parts[((size_t)blockIdx.x * SV_MAX_K + i) * kFitQ + j] = q[j];
+      for (int j = 1; j < kFitQ; ++j)
+        if (lane == j) v = q[j];
+      parts[((size_t)blockIdx.x * SV_MAX_K + i) * kFitQ + lane] = v;
     }
   }
   __syncthreads();
@@ -73,60 +80,73 @@ __global__ void avfit_kernel(const FitParams P) {
     s_last = (old == (uint32_t)G - 1u);
   }
   __syncthreads();
-  if (!s_last || threadIdx.x != 0) return;
+  if (!s_last || warp != 0) return;
   __threadfence();
-  hdr->cta_done = 0u;
 
-  // acc layout: g[0..K] (g[0] = slope), Hww, Hwb[K], Hbb[K], n[K]
+  // Last CTA, warp 0, lane i = position i: add the CTA partials (in CTA
+  // order) to the round accumulators, acc = [g (K+1; g[0] = slope), Hww,
+  // Hwb[K], Hbb[K], n[K]].
   double *g = acc;
   double *Hww = acc + (K + 1);
   double *Hwb = Hww + 1;
   double *Hbb = Hwb + K;
   double *n = Hbb + K;
-  for (int ii = 0; ii < K; ++ii) {
-    double t[kFitQ] = {0, 0, 0, 0, 0, 0};
+  double t[kFitQ] = {0, 0, 0, 0, 0, 0};
+  if (lane < K) {
     for (int c = 0; c < G; ++c)
-      for (int j = 0; j < kFitQ; ++j) t[j] += __ldcg(parts + ((size_t)c * SV_MAX_K + ii) * kFitQ + j);
-    g[0] += t[0];
-    *Hww += t[1];
-    g[1 + ii] += t[2];
-    Hwb[ii] += t[3];
-    Hbb[ii] += t[4];
-    n[ii] += t[5];
+#pragma unroll
+      for (int j = 0; j < kFitQ; ++j) t[j] += (double)__ldcg(parts + ((size_t)c * SV_MAX_K + lane) * kFitQ + j);
   }
-  hdr->step += 1u;
-  if ((int)hdr->step < P.round_len) return;
-
-  // End of round: damped Newton step over omega and the labelled intercepts.
-  double ntot = 0.0, trace = *Hww;
-  for (int ii = 0; ii < K; ++ii) {
-    ntot += n[ii];
-    trace += Hbb[ii];
+  double gb = 0, hwb = 0, hbb = 0, nn = 0;
+  if (lane < K) {
+    gb = __ldcg(g + 1 + lane) + t[2];
+    hwb = __ldcg(Hwb + lane) + t[3];
+    hbb = __ldcg(Hbb + lane) + t[4];
+    nn = __ldcg(n + lane) + t[5];
   }
-  if (ntot > 0.0) {
-    const double ridge = 1e-9 * trace / (double)(K + 1);
-    double a = *Hww + ridge, rhs = g[0];
-    for (int ii = 0; ii < K; ++ii) {
-      if (!(n[ii] > 0.0)) continue;
-      const double d = Hbb[ii] + ridge;
-      a -= Hwb[ii] * Hwb[ii] / d;
-      rhs -= Hwb[ii] * g[1 + ii] / d;
-    }
-    if (a > 0.0 && isfinite(rhs)) {
-      const double dw = rhs / a;
-      const double c = (double)P.damping_c;
-      P.theta[0] = (float)((double)P.theta[0] - ntot / (ntot + c) * dw);
-      for (int ii = 0; ii < K; ++ii) {
-        if (!(n[ii] > 0.0)) continue;
-        const double db = (g[1 + ii] - Hwb[ii] * dw) / (Hbb[ii] + ridge);
-        P.theta[1 + ii] = (float)((double)P.theta[1 + ii] - n[ii] / (n[ii] + c) * db);
+  const double gw = __ldcg(g) + warp_sum_d(t[0]);
+  const double hww = __ldcg(Hww) + warp_sum_d(t[1]);
+  const uint32_t step = hdr->step + 1u;
+  bool solved = false;
+  if ((int)step >= P.round_len) {
+    // End of round: damped Newton step over omega and the labelled intercepts
+    // (Schur complement of the arrow-shaped Hessian on omega).
+    const double ntot = warp_sum_d(nn);
+    const double trace = hww + warp_sum_d(hbb);
+    if (ntot > 0.0) {
+      const double ridge = 1e-9 * trace / (double)(K + 1);
+      const bool has = lane < K && nn > 0.0;
+      const double d = hbb + ridge;
+      const double s1 = warp_sum_d(has ? hwb * hwb / d : 0.0);
+      const double s2 = warp_sum_d(has ? hwb * gb / d : 0.0);
+      const double a = hww + ridge - s1, rhs = gw - s2;
+      if (a > 0.0 && isfinite(rhs)) {
+        const double dw = rhs / a;
+        const double c = (double)P.damping_c;
+        if (lane == 0) P.theta[0] = (float)((double)P.theta[0] - ntot / (ntot + c) * dw);
+        if (has) {
+          const double db = (gb - hwb * dw) / d;
+          P.theta[1 + lane] = (float)((double)P.theta[1 + lane] - nn / (nn + c) * db);
+        }
+      } else if (lane == 0) {
+        atomicOr(&hdr->status, SV_FLAG_FIT_SINGULAR);
       }
-    } else {
-      atomicOr(&hdr->status, SV_FLAG_FIT_SINGULAR);
     }
+    solved = true;
   }
-  for (int j = 0; j < (int)kAvAccDoubles; ++j) acc[j] = 0.0;
-  hdr->step = 0u;
+  // write the accumulators back (cleared at the end of a round)
+  if (lane < K) {
+    g[1 + lane] = solved ? 0.0 : gb;
+    Hwb[lane] = solved ? 0.0 : hwb;
+    Hbb[lane] = solved ? 0.0 : hbb;
+    n[lane] = solved ? 0.0 : nn;
+  }
+  if (lane == 0) {
+    g[0] = solved ? 0.0 : gw;
+    *Hww = solved ? 0.0 : hww;
+    hdr->step = solved ? 0u : step;
+    hdr->cta_done = 0u;
+  }
 }
 
 __global__ void philox_kernel(uint64_t seed, int nb, int npos, uint32_t *out) {

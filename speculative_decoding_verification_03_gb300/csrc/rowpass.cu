@@ -26,6 +26,7 @@
 #include <cfloat>
 #include <climits>
 
+#include "sample_common.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -35,21 +36,56 @@ namespace {
 
 constexpr int kFlagFirst = 1;
 constexpr int kFlagLast = 2;
+constexpr int kFlagDone = 4;
+constexpr int kFlagSample = 8;     // a residual/bonus item of the fused sampler
+constexpr int kFlagResidual = 16;  // ... whose stage also holds the draft row
+constexpr int kSampleHalfBytes = kStageBytes / 2;
+constexpr int kItemSample = -2;    // PartInfo.item of a finished sample item
 constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kEpilogueWarp = kConsumerWarps + 1;
+constexpr int kEpilogueWarp0 = kConsumerWarps + 1;  // .. + kEpiWarps - 1
 constexpr uint32_t kNegInfBf16x2 = 0xff80ff80u;
 constexpr uint32_t kNegInfF32 = 0xff800000u;
 
-struct StageHdr {
-  int item;  // -1: no more work
+// Per stage: the fields every math warp reads (one 16-byte shared load), the
+// sample parameters (sample stages only) and the item's metadata, read only
+// on the item's last stage.  A sample stage holds
+// target elements [e0, e0 + n) in its first half and, for a residual, the
+// draft row's same elements in its second half (n = nvec * 16 / esz).
+struct StageHot {
+  int e0;       // row element index of the first staged element
+  int nvec;     // staged 16-byte vectors (per half for a sample stage)
+  int flags;    // kFlagFirst | kFlagLast | kFlagDone | kFlagSample | kFlagResidual
+  float c;      // log2(e) / tau
+};
+
+struct StageSample {  // sample stages only
+  float nbt;    // weights 2^(z_t c + nbt)
+  float invtau;
+  float k0_hi, k0_lo;
+  int b;        // the sequence
+  int pad[3];
+};
+
+// Eight staged elements starting at element offset `off` of a stage half.
+template <int kDtype>
+__device__ __forceinline__ Raw8 smem_raw8(const uint8_t *half, int off) {
+  Raw8 r;
+  if (kDtype == SV_BF16) {
+    r.a = *reinterpret_cast<const uint4 *>(half + off * 2);
+    r.b = make_uint4(0, 0, 0, 0);
+  } else {
+    r.a = *reinterpret_cast<const uint4 *>(half + off * 4);
+    r.b = *reinterpret_cast<const uint4 *>(half + off * 4 + 16);
+  }
+  return r;
+}
+
+struct StageCold {
+  int item;
   int b;
   int sidx;   // statistics index inside the sequence: 2j (target j) or 2i+1 (draft i)
   int chunk;
-  int e0;     // row element index of the first staged element
-  int nvec;   // staged 16-byte vectors
-  int flags;
   int x0, xn0, x1, xn1;  // elements read with plain loads on the LAST stage
-  float c;               // log2(e) / tau
   long long row_off;     // element offset of the row inside its tensor
   int is_target;
   int pad;
@@ -73,13 +109,15 @@ struct alignas(16) Part {
 
 struct __align__(128) Smem {
   uint8_t ring[kStages][kStageBytes];
-  StageHdr hdr[kStages];
-  PartInfo pinfo[2];
-  Part part[2][kConsumerWarps];
+  StageHot hot[kStages];
+  StageSample smpl[kStages];
+  StageCold cold[kStages];
+  PartInfo pinfo[kPartSlots];
+  Part part[kPartSlots][kConsumerWarps];
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t pfull[2];
-  uint64_t pempty[2];
+  uint64_t pfull[kPartSlots];
+  uint64_t pempty[kPartSlots];
   int abort_flag;
 };
 
@@ -220,6 +258,14 @@ struct Elems<SV_BF16> {
     }
   }
   __device__ __forceinline__ static uint4 neg_inf() { return make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2); }
+  __device__ __forceinline__ static float vmax1(const uint4 &v) {
+    const uint32_t m = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
+    return fmaxf(bf16lo(m), bf16hi(m));
+  }
+  // element `local` of the staged data := -inf
+  __device__ __forceinline__ static void kill_smem(uint4 *ring, int local) {
+    reinterpret_cast<unsigned short *>(ring)[local] = (unsigned short)0xff80u;
+  }
   __device__ __forceinline__ static float vmax(const uint4 (&w)[kVecPerThread]) {
     uint32_t m0 = bf16x2_max(w[0].x, w[0].y), m1 = bf16x2_max(w[0].z, w[0].w);
 #pragma unroll
@@ -248,6 +294,12 @@ struct Elems<SV_FP32> {
     }
   }
   __device__ __forceinline__ static uint4 neg_inf() { return make_uint4(kNegInfF32, kNegInfF32, kNegInfF32, kNegInfF32); }
+  __device__ __forceinline__ static float vmax1(const uint4 &v) {
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+  __device__ __forceinline__ static void kill_smem(uint4 *ring, int local) {
+    reinterpret_cast<uint32_t *>(ring)[local] = kNegInfF32;
+  }
   __device__ __forceinline__ static float vmax(const uint4 (&w)[kVecPerThread]) {
     float m = -INFINITY;
 #pragma unroll
@@ -258,43 +310,85 @@ struct Elems<SV_FP32> {
   }
 };
 
-// One staged block of vectors: vector j of this lane is vector (tid + j * kConsumers)
-// of the stage, its element k sits at row index e0 + vi * kPerVec + k.
+// The running-max raise.  vm[j] is the max of this lane's vector j (pass 1);
+// the lane's first element equal to wm lies in its first vector with
+// vm[j] == wm.  The lane owning the first copy of wm overwrites it with -inf
+// in shared memory (the stage is this warp's until released, and only this
+// lane reads that vector), then the lane sums are rescaled.
 template <int kDtype>
-__device__ __forceinline__ void consume_vectors(WarpState &s, uint4 (&w)[kVecPerThread], int tid, int lane, int e0,
-                                                float c) {
+__device__ __forceinline__ void stage_rise(WarpState &s, uint4 *ring, const float (&vm)[kVecPerThread], int tid,
+                                           int lane, int e0, float c, float wm) {
   using E = Elems<kDtype>;
-  const float wm = warp_max(E::vmax(w));
-  if (wm > s.M) {  // warp-uniform
-    int cand = INT_MAX;
+  int jv = -1;
 #pragma unroll
-    for (int j = kVecPerThread - 1; j >= 0; --j)
+  for (int j = kVecPerThread - 1; j >= 0; --j)
+    if (vm[j] == wm) jv = j;
+  int cand = INT_MAX;
+  if (jv >= 0) {
+    const int vi = tid + jv * kConsumers;
+    const uint4 v = ring[vi];
+    int k0 = E::kPerVec - 1;
 #pragma unroll
-      for (int k = E::kPerVec - 1; k >= 0; --k)
-        if (E::get(w[j], k) == wm) cand = e0 + (tid + j * kConsumers) * E::kPerVec + k;
-    const int gidx = warp_min_i(cand);
-    if (cand == gidx) {
-#pragma unroll
-      for (int j = 0; j < kVecPerThread; ++j)
-#pragma unroll
-        for (int k = 0; k < E::kPerVec; ++k)
-          if (e0 + (tid + j * kConsumers) * E::kPerVec + k == gidx) E::kill(w[j], k);
-    }
-    state_rise(s, wm, gidx, c, lane);
+    for (int k = E::kPerVec - 2; k >= 0; --k)
+      if (E::get(v, k) == wm) k0 = k;
+    cand = e0 + vi * E::kPerVec + k0;
   }
-  float acc = 0.f;
+  const int gidx = warp_min_i(cand);
+  if (cand == gidx) E::kill_smem(ring, gidx - e0);
+  __syncwarp();
+  state_rise(s, wm, gidx, c, lane);
+}
+
+// exp2 terms of one 16-byte vector in packed pairs: fma2 for the arguments,
+// two MUFU ex2, add2 into four pair accumulators.
+template <int kDtype>
+__device__ __forceinline__ void vec_exp_acc(const uint4 &v, float2 cc, float2 nb, float2 (&acc)[4]) {
+  using E = Elems<kDtype>;
 #pragma unroll
-  for (int j = 0; j < kVecPerThread; ++j) {
-    float t[E::kPerVec];
-#pragma unroll
-    for (int k = 0; k < E::kPerVec; ++k) t[k] = ex2_approx(fmaf(E::get(w[j], k), c, s.nbh));
-#pragma unroll
-    for (int h = E::kPerVec / 2; h > 0; h >>= 1)
-#pragma unroll
-      for (int k = 0; k < h; ++k) t[k] += t[k + h];
-    acc += t[0];
+  for (int p = 0; p < E::kPerVec / 2; ++p) {
+    float2 t = __ffma2_rn(make_float2(E::get(v, 2 * p), E::get(v, 2 * p + 1)), cc, nb);
+    t.x = ex2_approx(t.x);
+    t.y = ex2_approx(t.y);
+    acc[p & 3] = __fadd2_rn(acc[p & 3], t);
   }
-  s.A += acc;
+}
+
+// One stage in shared memory, read twice: vector j of this lane is vector
+// vi = tid + j * kConsumers of the stage, its element k sits at row index
+// e0 + vi * kPerVec + k.  Pass 1 takes the stage max (and raises the warp max
+// when needed, see stage_rise), pass 2 sums the exp2 terms.  Full stages take
+// a path without per-vector bounds checks.
+template <int kDtype>
+__device__ __forceinline__ void consume_stage(WarpState &s, uint4 *ring, int nvec, int tid, int lane, int e0,
+                                              float c) {
+  using E = Elems<kDtype>;
+  const uint4 *base = ring + tid;
+  float vm[kVecPerThread];
+  const bool full = nvec == kVecPerStage;
+  if (full) {
+#pragma unroll
+    for (int j = 0; j < kVecPerThread; ++j) vm[j] = E::vmax1(base[j * kConsumers]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kVecPerThread; ++j)
+      vm[j] = (tid + j * kConsumers < nvec) ? E::vmax1(base[j * kConsumers]) : -INFINITY;
+  }
+  float lm = vm[0];
+#pragma unroll
+  for (int j = 1; j < kVecPerThread; ++j) lm = fmaxf(lm, vm[j]);
+  const float wm = warp_max(lm);
+  if (wm > s.M) stage_rise<kDtype>(s, ring, vm, tid, lane, e0, c, wm);  // warp-uniform
+  const float2 cc = make_float2(c, c), nb = make_float2(s.nbh, s.nbh);
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  if (full) {
+#pragma unroll
+    for (int j = 0; j < kVecPerThread; ++j) vec_exp_acc<kDtype>(base[j * kConsumers], cc, nb, acc);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kVecPerThread; ++j)
+      if (tid + j * kConsumers < nvec) vec_exp_acc<kDtype>(base[j * kConsumers], cc, nb, acc);
+  }
+  s.A += ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
 }
 
 // Scalar elements (ragged row ends): one value per lane, index idx.
@@ -330,13 +424,26 @@ __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
   }
   const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
 
+  // Lane i <= k: ln S of target row i; lane i < k: ln S of draft row i, the
+  // acceptance test at position i, the AV feature and confidence.
   bool reject = false;
   int d = -1;
+  double lnSt = 0.0, lnSd = 0.0;
+  Part T, D;
+  T.m = D.m = 0.f;
+  T.E = D.E = 0.f;
+  T.arg = D.arg = 0;
+  T.flags = D.flags = 0u;
+  if (lane <= k) {
+    T = load_stats_cg(st + 2 * lane);
+    lnSt = log1p((double)T.E);
+    flags |= T.flags & SV_FLAG_NONFINITE;
+  }
   if (lane < k) {
     const int i = lane;
-    const Part T = load_stats_cg(st + 2 * i);
-    const Part D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + i) : load_stats_cg(st + 2 * i + 1);
-    flags |= (T.flags | D.flags) & SV_FLAG_NONFINITE;
+    D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + i) : load_stats_cg(st + 2 * i + 1);
+    lnSd = log1p((double)D.E);
+    flags |= D.flags & SV_FLAG_NONFINITE;
     d = __ldg(P.draft_tokens + (size_t)b * K + i);
     const bool in_range = d >= 0 && d < P.V;
     if (!in_range) flags |= SV_FLAG_TOKEN_RANGE;
@@ -350,11 +457,11 @@ __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
         const long long drow = ((long long)b * K + i) * (long long)rowb;
         const double zt = (double)logit_at(P.target, P.dtype, trow + d);
         const double zd = (double)logit_at(P.draft, P.dtype, drow + d);
-        const double lq = (zd - (double)D.m) * invtau - log1p((double)D.E);
+        const double lq = (zd - (double)D.m) * invtau - lnSd;
         if (lq == -INFINITY) {
           ratio = INFINITY;
         } else {
-          const double lp = (zt - (double)T.m) * invtau - log1p((double)T.E);
+          const double lp = (zt - (double)T.m) * invtau - lnSt;
           ratio = exp(lp - lq);
         }
       }
@@ -377,13 +484,19 @@ __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
   const unsigned rej = __ballot_sync(0xffffffffu, reject);
   const int a = rej ? (__ffs(rej) - 1) : k;
 
+  // Row a's statistics from lane a.
+  const float Ta_m = __shfl_sync(0xffffffffu, T.m, a);
+  const int Ta_arg = __shfl_sync(0xffffffffu, T.arg, a);
+  const double lnSt_a = __shfl_sync(0xffffffffu, lnSt, a);
+  const float Da_m = __shfl_sync(0xffffffffu, D.m, a);
+  const double lnSd_a = __shfl_sync(0xffffffffu, lnSd, a);
+
   // Emitted tokens: accepted drafts, the position-a token (written here for
   // greedy rows, by the sampler otherwise), then -1.
-  const Part Ta = load_stats_cg(st + 2 * a);
   if (lane <= K) {
     int32_t v = -1;
     if (lane < a) v = d;
-    else if (lane == a && greedy) v = (Ta.arg >= 0 && Ta.arg < P.V) ? Ta.arg : 0;
+    else if (lane == a && greedy) v = (Ta_arg >= 0 && Ta_arg < P.V) ? Ta_arg : 0;
     P.out_tokens[(size_t)b * (K + 1) + lane] = v;
   }
   if (lane == 0) {
@@ -391,21 +504,27 @@ __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
     SampleTask t;
     t.kind = greedy ? kTaskNone : (a < k ? kTaskResidual : kTaskBonus);
     t.a = a;
-    t.argmax_t = (Ta.arg >= 0 && Ta.arg < P.V) ? Ta.arg : 0;
+    t.argmax_t = (Ta_arg >= 0 && Ta_arg < P.V) ? Ta_arg : 0;
     t.c = (float)(kLog2ed * invtau);
     t.invtau = (float)invtau;
-    const double lnSt = log1p((double)Ta.E);
-    t.nbt = (float)(-((double)Ta.m * (kLog2ed * invtau) + lnSt * kLog2ed));
+    t.nbt = (float)(-((double)Ta_m * (kLog2ed * invtau) + lnSt_a * kLog2ed));
     t.k0_hi = 0.f;
     t.k0_lo = 0.f;
     if (t.kind == kTaskResidual) {
-      const Part Da = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + a) : load_stats_cg(st + 2 * a + 1);
-      const double k0 = ((double)Ta.m - (double)Da.m) * invtau + lnSt - log1p((double)Da.E);
+      const double k0 = ((double)Ta_m - (double)Da_m) * invtau + lnSt_a - lnSd_a;
       t.k0_hi = (float)k0;
       t.k0_lo = (float)(k0 - (double)t.k0_hi);
     }
     t.u = greedy ? 0.0 : uniform24(P.seed, (uint32_t)b, (uint32_t)a, 1);
     P.tasks[b] = t;
+    if (P.fused) {
+      // hand the sequence's sample items to the producers (all sp of them,
+      // also for greedy rows, so that every slot gets an item); the fence
+      // orders the task before the entries
+      __threadfence();
+      const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)P.sp);
+      for (int q = 0; q < P.sp; ++q) st_relaxed_gpu(P.dq + base + q, b * P.sp + q + 1);
+    }
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0 && flags) atomicOr(P.status, flags);
@@ -465,7 +584,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
       mbar_init(&S.full[s], 1);
       mbar_init(&S.empty[s], kConsumerWarps);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kPartSlots; ++s) {
       mbar_init(&S.pfull[s], kConsumerWarps);
       mbar_init(&S.pempty[s], 1);
     }
@@ -487,9 +606,126 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
     float cached_c = 1.f;
     bool ok = true;
     const int K = P.K;
+    // Static row tickets are fetched one item ahead, so the atomic's round
+    // trip overlaps the staging of the current item.  Sample items are
+    // claimed with one atomicAdd each (a unique slot, no retries); a claimed
+    // slot whose entry is not yet published stays pending while row items
+    // continue, and is waited on (bounded) only when no row item is left.
+    bool static_left = true, dyn_left = P.fused != 0;
+    int next_static = (int)atomicAdd(P.ticket, 1u);
+    int pending = -1;   // claimed sample slot, not yet taken
+    int pend_val = 0;   // its entry as last read (one item ahead)
+    int q_head = 0, q_tail = 0;
+    if (P.fused) {
+      q_head = ld_relaxed_gpu(reinterpret_cast<const int *>(P.dq_head));
+      q_tail = ld_relaxed_gpu(reinterpret_cast<const int *>(P.dq_tail));
+    }
     for (;;) {
-      const int item = (int)atomicAdd(P.ticket, 1u);
-      if (item >= P.nitems) break;
+      int dyn = -1;
+      if (dyn_left) {
+        if (pending < 0 && (q_head < q_tail || !static_left)) {
+          const int c = (int)atomicAdd(P.dq_head, 1u);
+          if (c < P.ndyn) {
+            pending = c;
+            pend_val = ld_relaxed_gpu(P.dq + c);
+          } else {
+            dyn_left = false;
+          }
+        }
+        if (pending >= 0 && (pend_val != 0 || !static_left)) {
+          dyn = pending;  // published, or nothing else to do: wait for it below
+          pending = -1;
+        }
+        // queue state for the next decision, read while this item is staged
+        q_head = ld_relaxed_gpu(reinterpret_cast<const int *>(P.dq_head));
+        q_tail = ld_relaxed_gpu(reinterpret_cast<const int *>(P.dq_tail));
+        if (pending >= 0) pend_val = ld_relaxed_gpu(P.dq + pending);
+      }
+      int item;
+      if (dyn >= 0) {
+        item = P.nstatic + dyn;
+      } else {
+        if (!static_left) {
+          if (dyn_left) continue;
+          break;
+        }
+        item = next_static;
+        if (item >= P.nstatic) {
+          static_left = false;
+          continue;
+        }
+        next_static = (int)atomicAdd(P.ticket, 1u);
+      }
+      if (item >= P.nstatic) {
+        // ---- a sample item: its slot is reserved; wait (bounded) for the entry
+        const int* slot = P.dq + (item - P.nstatic);
+        int code = ld_acquire_gpu(slot);
+        if (code == 0) {
+          const uint64_t t0 = global_ns();
+          while ((code = ld_acquire_gpu(slot)) == 0) {
+            if (*abort_flag) break;
+            if (global_ns() - t0 > P.timeout_ns) {
+              *abort_flag = 1;
+              atomicOr(P.status, SV_FLAG_TIMEOUT);
+              break;
+            }
+            __nanosleep(200);
+          }
+          if (code == 0) {
+            ok = false;
+            break;
+          }
+        }
+        --code;
+        const int b = code / P.sp, part = code - (code / P.sp) * P.sp;
+        const SampleTask t = load_task_cg(P.tasks + b);
+        if (t.kind == kTaskNone) continue;
+        const bool resid = t.kind == kTaskResidual;
+        const long long t_off = ((long long)b * (K + 1) + t.a) * (long long)P.V;
+        const long long d_off = ((long long)b * K + t.a) * (long long)P.V;
+        const int j0 = part * P.spc, j1 = min(P.smp.nsub, j0 + P.spc);
+        const int e_beg = min(P.V, j0 * kSubChunk), e_end = min(P.V, j1 * kSubChunk);
+        const int half_elems = kSampleHalfBytes / kEsz;
+        const int nst = e_end > e_beg ? (e_end - e_beg + half_elems - 1) / half_elems : 1;
+        for (int st = 0; st < nst; ++st) {
+          if (!mbar_wait_bounded(&S.empty[s], phase ^ 1u, abort_flag, P.status, P.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          const int e = e_beg + st * half_elems;
+          const int n = max(0, min(half_elems, e_end - e));
+          const int bytes = n * kEsz;  // a multiple of 16: rows are 16-byte aligned on this path
+          StageHot &h = S.hot[s];
+          h.e0 = e;
+          h.nvec = bytes / 16;
+          h.flags = kFlagSample | (resid ? kFlagResidual : 0) | (st == 0 ? kFlagFirst : 0) |
+                    (st == nst - 1 ? kFlagLast : 0);
+          h.c = t.c;
+          StageSample &hs = S.smpl[s];
+          hs.nbt = t.nbt;
+          hs.invtau = t.invtau;
+          hs.k0_hi = t.k0_hi;
+          hs.k0_lo = t.k0_lo;
+          hs.b = b;
+          ++nfull[s];
+          if (bytes > 0) {
+            mbar_arrive_expect_tx(&S.full[s], (uint32_t)(resid ? 2 * bytes : bytes));
+            bulk_g2s(S.ring[s], reinterpret_cast<const char *>(P.target) + (t_off + e) * kEsz, (uint32_t)bytes,
+                     &S.full[s]);
+            if (resid)
+              bulk_g2s(S.ring[s] + kSampleHalfBytes, reinterpret_cast<const char *>(P.draft) + (d_off + e) * kEsz,
+                       (uint32_t)bytes, &S.full[s]);
+          } else {
+            mbar_arrive(&S.full[s]);
+          }
+          if (++s == kStages) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        continue;
+      }
       const int per_seq = P.nslot * P.nch;
       const int b = item / per_seq;
       const int rem = item - b * per_seq;
@@ -537,21 +773,24 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
         }
         const long long off_b = (long long)st * kStageBytes;
         const int bytes = mid_bytes > 0 ? (int)min((long long)kStageBytes, mid_bytes - off_b) : 0;
-        StageHdr &h = S.hdr[s];
-        h.item = item;
-        h.b = b;
-        h.sidx = sidx;
-        h.chunk = chunk;
+        StageHot &h = S.hot[s];
         h.e0 = a0 + (int)(off_b / kEsz);
         h.nvec = bytes / 16;
         h.flags = (st == 0 ? kFlagFirst : 0) | (st == nst - 1 ? kFlagLast : 0);
-        h.x0 = x0;
-        h.xn0 = xn0;
-        h.x1 = x1;
-        h.xn1 = xn1;
         h.c = cached_c;
-        h.row_off = row_off;
-        h.is_target = is_target;
+        if (st == nst - 1) {
+          StageCold &cd = S.cold[s];
+          cd.item = item;
+          cd.b = b;
+          cd.sidx = sidx;
+          cd.chunk = chunk;
+          cd.x0 = x0;
+          cd.xn0 = xn0;
+          cd.x1 = x1;
+          cd.xn1 = xn1;
+          cd.row_off = row_off;
+          cd.is_target = is_target;
+        }
         ++nfull[s];
         if (bytes > 0) {
           mbar_arrive_expect_tx(&S.full[s], (uint32_t)bytes);
@@ -567,7 +806,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
       if (!ok) break;
     }
     if (ok && mbar_wait_bounded(&S.empty[s], phase ^ 1u, abort_flag, P.status, P.timeout_ns)) {
-      S.hdr[s].item = -1;
+      S.hot[s].flags = kFlagDone;
       ++nfull[s];
       mbar_arrive(&S.full[s]);
     } else {
@@ -583,13 +822,35 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
     return;
   }
 
-  if (warp == kEpilogueWarp) {
+  if (warp >= kEpilogueWarp0) {
     // ------------------------------------------------------------------ epilogue
     const int K = P.K;
-    for (int it = 0;; ++it) {
-      const int slot = it & 1;
-      if (!mbar_wait_bounded(&S.pfull[slot], (uint32_t)((it >> 1) & 1), abort_flag, P.status, P.timeout_ns)) break;
+    // items alternate between the epilogue warps: this one takes items
+    // n = e, e + kEpiWarps, ... in slots n % kPartSlots
+    for (int it = warp - kEpilogueWarp0;; it += kEpiWarps) {
+      const int slot = it % kPartSlots;
+      if (!mbar_wait_bounded(&S.pfull[slot], (uint32_t)((it / kPartSlots) & 1), abort_flag, P.status, P.timeout_ns)) break;
       const PartInfo info = S.pinfo[slot];
+      if (info.item == kItemSample) {
+        // a sample item of sequence info.b finished: the last of its sp items
+        // locates the token
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.pempty[slot]);
+        int last = 0;
+        if (lane == 0) {
+          __threadfence();
+          last = atomicAdd(P.smp.smp_cnt + info.b, 1u) == (uint32_t)P.sp - 1u;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          const SampleTask t = load_task_cg(P.tasks + info.b);
+          const RowPtrs R = row_ptrs(P.smp, t, info.b, P.esz);
+          if (P.dtype == SV_BF16) finalize_warp<SV_BF16>(P.smp, t, info.b, R, lane);
+          else finalize_warp<SV_FP32>(P.smp, t, info.b, R, lane);
+        }
+        continue;
+      }
       if (info.item < 0) break;
       Part mine = {-INFINITY, 0.f, INT_MAX, 0u};
       if (lane < kConsumerWarps) mine = S.part[slot][lane];
@@ -653,47 +914,102 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
   float c = 1.f;
   for (;;) {
     if (!mbar_wait_bounded(&S.full[s], phase, abort_flag, P.status, P.timeout_ns)) break;
-    const StageHdr h = S.hdr[s];
-    if (h.item < 0) {
+    const StageHot h = S.hot[s];
+    if (h.flags & kFlagDone) {
       // propagate the end of work to the epilogue warp
-      const int slot = it & 1;
-      if (mbar_wait_bounded(&S.pempty[slot], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag, P.status, P.timeout_ns)) {
+      // one end-of-work marker for each epilogue warp (consecutive items)
+      for (int e = 0; e < kEpiWarps; ++e, ++it) {
+        const int slot = it % kPartSlots;
+        if (!mbar_wait_bounded(&S.pempty[slot], (uint32_t)(((it / kPartSlots) & 1) ^ 1), abort_flag, P.status,
+                               P.timeout_ns))
+          break;
         if (warp == 0 && lane == 0) S.pinfo[slot].item = -1;
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.pfull[slot]);
       }
       break;
     }
+    if (h.flags & kFlagSample) {
+      // Residual / bonus weights of the staged elements, summed per 256-element
+      // sub-chunk (one sub-chunk per warp pass, 8 elements per lane).
+      const StageSample hs = S.smpl[s];
+      SampleTask t;
+      t.kind = (h.flags & kFlagResidual) ? kTaskResidual : kTaskBonus;
+      t.c = h.c;
+      t.nbt = hs.nbt;
+      t.invtau = hs.invtau;
+      t.k0_hi = hs.k0_hi;
+      t.k0_lo = hs.k0_lo;
+      const int n = h.nvec * 16 / kEsz;
+      const int nsc = (n + kSubChunk - 1) / kSubChunk;
+      float *sub = P.smp.subsum + (size_t)hs.b * P.smp.nsub + h.e0 / kSubChunk;
+      for (int q = warp; q < nsc; q += kConsumerWarps) {
+        const int off = q * kSubChunk + lane * 8;  // element offset inside the stage
+        const Raw8 zt = smem_raw8<kDtype>(S.ring[s], off);
+        Raw8 zd;
+        zd.a = zd.b = make_uint4(0, 0, 0, 0);
+        if (t.kind == kTaskResidual) zd = smem_raw8<kDtype>(S.ring[s] + kSampleHalfBytes, off);
+        float r[8];
+        weights_from<kDtype>(t, t.kind, off, n, zt, zd, r);
+        const float sm = warp_sum(sum8(r));
+        if (lane == 0) sub[q] = sm;
+      }
+      const bool last = (h.flags & kFlagLast) != 0;
+      const int bb = hs.b;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[s]);
+      if (last) {
+        if (lane == 0) __threadfence();  // sub-chunk sums visible before the completion count
+        const int slot = it % kPartSlots;
+        if (!mbar_wait_bounded(&S.pempty[slot], (uint32_t)(((it / kPartSlots) & 1) ^ 1), abort_flag, P.status,
+                               P.timeout_ns))
+          break;
+        if (warp == 0 && lane == 0) {
+          PartInfo pi;
+          pi.item = kItemSample;
+          pi.b = bb;
+          pi.sidx = 0;
+          pi.chunk = 0;
+          pi.c = 0.f;
+          S.pinfo[slot] = pi;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.pfull[slot]);
+        ++it;
+      }
+      if (++s == kStages) {
+        s = 0;
+        phase ^= 1u;
+      }
+      continue;
+    }
     if (h.flags & kFlagFirst) {
       state_reset(st);
       c = h.c;
     }
-    uint4 w[kVecPerThread];
-    const uint4 *ring = reinterpret_cast<const uint4 *>(S.ring[s]);
-#pragma unroll
-    for (int j = 0; j < kVecPerThread; ++j) {
-      const int vi = tid + j * kConsumers;
-      w[j] = vi < h.nvec ? ring[vi] : Elems<kDtype>::neg_inf();
-    }
+    StageCold cd;
+    if (h.flags & kFlagLast) cd = S.cold[s];
+    if (h.nvec > 0) consume_stage<kDtype>(st, reinterpret_cast<uint4 *>(S.ring[s]), h.nvec, tid, lane, h.e0, c);
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[s]);
-    if (h.nvec > 0) consume_vectors<kDtype>(st, w, tid, lane, h.e0, c);
 
     if (h.flags & kFlagLast) {
       if (warp == 0) {
-        const int nx = h.xn0 + h.xn1;
+        const int nx = cd.xn0 + cd.xn1;
         if (nx > 0) {
-          const int idx = lane < h.xn0 ? h.x0 + lane : h.x1 + (lane - h.xn0);
-          const void *base = h.is_target ? P.target : P.draft;
-          const float v = lane < nx ? logit_at(base, kDtype, h.row_off + idx) : -INFINITY;
+          const int idx = lane < cd.xn0 ? cd.x0 + lane : cd.x1 + (lane - cd.xn0);
+          const void *base = cd.is_target ? P.target : P.draft;
+          const float v = lane < nx ? logit_at(base, kDtype, cd.row_off + idx) : -INFINITY;
           consume_scalar(st, v, idx, lane, c);
         }
       }
       // warp partial: lane sums in true units, then across the warp
       const float T = st.A * fmaf(st.nbl, kLn2, 1.0f);
       const float Ew = warp_sum(T);
-      const int slot = it & 1;
-      if (!mbar_wait_bounded(&S.pempty[slot], (uint32_t)(((it >> 1) & 1) ^ 1), abort_flag, P.status, P.timeout_ns)) break;
+      const int slot = it % kPartSlots;
+      if (!mbar_wait_bounded(&S.pempty[slot], (uint32_t)(((it / kPartSlots) & 1) ^ 1), abort_flag, P.status,
+                             P.timeout_ns))
+        break;
       if (lane == 0) {
         Part pr;
         pr.m = st.M;
@@ -703,10 +1019,10 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
         S.part[slot][warp] = pr;
         if (warp == 0) {
           PartInfo pi;
-          pi.item = h.item;
-          pi.b = h.b;
-          pi.sidx = h.sidx;
-          pi.chunk = h.chunk;
+          pi.item = cd.item;
+          pi.b = cd.b;
+          pi.sidx = cd.sidx;
+          pi.chunk = cd.chunk;
           pi.c = c;
           S.pinfo[slot] = pi;
         }

@@ -1,0 +1,281 @@
+// Residual / bonus weights and the per-sequence inverse-CDF finalisation,
+// shared by the fused row-pass kernel and the standalone sampler.
+//
+// "Speculative Decoding: Draft, EAGLE, MTP", section "one speculative step":
+// at the first rejection a the emitted token is drawn from the normalised
+// positive residual max(p_a - q_a, 0); when every verified draft passed, the
+// bonus token is drawn from p_k.  The token is the smallest v with
+// C(v) > u * R, C the running sum of the weights in vocabulary order and R
+// their total.  Weights: p_v = 2^(z_t c + nbt) up to a common factor (which
+// cancels in C(v) / R); residual r_v = p_v * (1 - e^delta_v) where
+// delta_v = ln q_v - ln p_v < 0, with 1 - e^delta from a Taylor polynomial
+// near 0 so that nearly equal p and q do not cancel.
+#pragma once
+
+#include <climits>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+
+// -(e^d - 1) for |d| <= 0.25 from the Taylor series of e^d - 1 truncated
+// after d^7 / 7! (relative truncation error below 4e-9 on that interval).
+__device__ __forceinline__ float one_minus_exp_small(float d) {
+  float p = 1.f / 5040.f;
+  p = fmaf(p, d, 1.f / 720.f);
+  p = fmaf(p, d, 1.f / 120.f);
+  p = fmaf(p, d, 1.f / 24.f);
+  p = fmaf(p, d, 1.f / 6.f);
+  p = fmaf(p, d, 0.5f);
+  p = fmaf(p, d, 1.f);
+  return -(p * d);
+}
+
+// Eight logits v0..v0+7 of a row as raw bits (bf16: one uint4; fp32: two).
+struct Raw8 {
+  uint4 a, b;
+};
+
+template <int kDtype>
+__device__ __forceinline__ Raw8 load8(const void *base, long long row_off, int v0, int V, bool vec_ok) {
+  Raw8 r;
+  if (kDtype == SV_BF16) {
+    const unsigned short *p = reinterpret_cast<const unsigned short *>(base) + row_off;
+    if (vec_ok && v0 + 8 <= V) {
+      r.a = __ldg(reinterpret_cast<const uint4 *>(p + v0));
+    } else {
+      uint32_t h[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) h[k] = (v0 + k < V) ? (uint32_t)__ldg(p + v0 + k) : 0u;
+      r.a = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+    }
+    r.b = make_uint4(0, 0, 0, 0);
+  } else {
+    const float *p = reinterpret_cast<const float *>(base) + row_off;
+    if (vec_ok && v0 + 8 <= V) {
+      r.a = __ldg(reinterpret_cast<const uint4 *>(p + v0));
+      r.b = __ldg(reinterpret_cast<const uint4 *>(p + v0 + 4));
+    } else {
+      uint32_t h[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) h[k] = (v0 + k < V) ? __float_as_uint(__ldg(p + v0 + k)) : 0u;
+      r.a = make_uint4(h[0], h[1], h[2], h[3]);
+      r.b = make_uint4(h[4], h[5], h[6], h[7]);
+    }
+  }
+  return r;
+}
+
+template <int kDtype>
+__device__ __forceinline__ float raw_at(const Raw8 &r, int k) {
+  if (kDtype == SV_BF16) {
+    const uint32_t w = (k >> 1) == 0 ? r.a.x : (k >> 1) == 1 ? r.a.y : (k >> 1) == 2 ? r.a.z : r.a.w;
+    return (k & 1) ? bf16hi(w) : bf16lo(w);
+  }
+  const uint4 &q = k < 4 ? r.a : r.b;
+  const int kk = k & 3;
+  return __uint_as_float(kk == 0 ? q.x : kk == 1 ? q.y : kk == 2 ? q.z : q.w);
+}
+
+// A task written by another SM during the same kernel: read it from L2.
+__device__ __forceinline__ SampleTask load_task_cg(const SampleTask *p) {
+  static_assert(sizeof(SampleTask) % 8 == 0, "SampleTask is read as 8-byte words");
+  SampleTask t;
+  const int2 *src = reinterpret_cast<const int2 *>(p);
+  int2 *dst = reinterpret_cast<int2 *>(&t);
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(SampleTask) / 8); ++i) dst[i] = __ldcg(src + i);
+  return t;
+}
+
+struct RowPtrs {
+  long long t_off, d_off;
+  bool t_vec, d_vec;
+};
+
+// Weights of the eight elements v0..v0+7.
+template <int kDtype>
+__device__ __forceinline__ void weights_from(const SampleTask &t, int kind, int v0, int V, const Raw8 &zt,
+                                             const Raw8 &zd, float (&r)[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float a = raw_at<kDtype>(zt, k);
+    const float p = ex2_approx(fmaf(a, t.c, t.nbt));
+    float w = p;
+    if (kind == kTaskResidual) {
+      const float delta = fmaf(raw_at<kDtype>(zd, k) - a, t.invtau, t.k0_hi) + t.k0_lo;
+      const float om = delta > -0.25f ? one_minus_exp_small(delta) : 1.f - ex2_approx(delta * kLog2e);
+      w = (p > 0.f && delta < 0.f) ? p * om : 0.f;
+    }
+    r[k] = (v0 + k < V) ? w : 0.f;
+  }
+}
+
+template <int kDtype>
+__device__ __forceinline__ void weights8(const SampleParams &P, const SampleTask &t, int kind, const RowPtrs &R, int j,
+                                         int lane, float (&r)[8]) {
+  const int v0 = j * kSubChunk + lane * 8;
+  const Raw8 zt = load8<kDtype>(P.target, R.t_off, v0, P.V, R.t_vec);
+  Raw8 zd;
+  zd.a = zd.b = make_uint4(0, 0, 0, 0);
+  if (kind == kTaskResidual) zd = load8<kDtype>(P.draft, R.d_off, v0, P.V, R.d_vec);
+  weights_from<kDtype>(t, kind, v0, P.V, zt, zd, r);
+}
+
+__device__ __forceinline__ float sum8(const float (&r)[8]) {
+  return ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+}
+
+__device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+__device__ __forceinline__ RowPtrs row_ptrs(const SampleParams &P, const SampleTask &t, int b, int esz) {
+  RowPtrs R;
+  R.t_off = ((long long)b * (P.K + 1) + t.a) * (long long)P.V;
+  R.d_off = ((long long)b * P.K + t.a) * (long long)P.V;
+  R.t_vec = ((reinterpret_cast<uintptr_t>(P.target) + (uintptr_t)R.t_off * esz) & 15) == 0;
+  R.d_vec = t.kind == kTaskResidual && ((reinterpret_cast<uintptr_t>(P.draft) + (uintptr_t)R.d_off * esz) & 15) == 0;
+  return R;
+}
+
+// One warp: sums of sub-chunks [j0, j1) (at most kSampleUnroll), loads first.
+template <int kDtype>
+__device__ __forceinline__ void group_sums(const SampleParams &P, const SampleTask &t, int kind, const RowPtrs &R,
+                                           int j0, int j1, int lane, float *subsum) {
+  Raw8 zt[kSampleUnroll], zd[kSampleUnroll];
+#pragma unroll
+  for (int u = 0; u < kSampleUnroll; ++u) {
+    const int v0 = (j0 + u) * kSubChunk + lane * 8;
+    zd[u].a = zd[u].b = zt[u].a = zt[u].b = make_uint4(0, 0, 0, 0);
+    if (j0 + u < j1) {
+      zt[u] = load8<kDtype>(P.target, R.t_off, v0, P.V, R.t_vec);
+      if (kind == kTaskResidual) zd[u] = load8<kDtype>(P.draft, R.d_off, v0, P.V, R.d_vec);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kSampleUnroll; ++u) {
+    if (j0 + u < j1) {
+      float r[8];
+      weights_from<kDtype>(t, kind, (j0 + u) * kSubChunk + lane * 8, P.V, zt[u], zd[u], r);
+      const float s = warp_sum(sum8(r));
+      if (lane == 0) subsum[j0 + u] = s;
+    }
+  }
+}
+
+// One warp locates the token of sequence b from its sub-chunk sums.  Lane l
+// owns sub-chunks [l q, l q + q); when q <= kFinalRegs they are read once into
+// registers.  Prefix sums across sub-chunks are fp64 (a prefix error of
+// 1e-7 R would move the crossing at large V); inside the crossing sub-chunk
+// the prefix is fp32 from the sub-chunk's start.
+constexpr int kFinalRegs = 24;
+
+template <int kDtype>
+__device__ void finalize_warp(const SampleParams &P, const SampleTask &t, int b, const RowPtrs &R, int lane) {
+  float *sub = P.subsum + (size_t)b * P.nsub;
+  const int nsub = P.nsub;
+  const int q = (nsub + 31) / 32;
+  const int ja = min(nsub, lane * q), jb = min(nsub, ja + q);
+  const bool in_regs = q <= kFinalRegs;
+  int kind = t.kind;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    float v[kFinalRegs];
+    double mine = 0.0;
+    if (in_regs) {
+#pragma unroll
+      for (int u = 0; u < kFinalRegs; ++u) v[u] = (ja + u < jb) ? __ldcg(sub + ja + u) : 0.f;
+#pragma unroll
+      for (int u = 0; u < kFinalRegs; ++u) mine += (double)v[u];
+    } else {
+      for (int j = ja; j < jb; ++j) mine += (double)__ldcg(sub + j);
+    }
+    const double incl = warp_incl_scan_d(mine, lane);
+    const double Rtot = __shfl_sync(0xffffffffu, incl, 31);
+    const double excl = incl - mine;
+    if (!(Rtot > 0.0) && kind == kTaskResidual && attempt == 0) {
+      // Zero residual mass (rounding only): sample p_a instead, and say so.
+      if (lane == 0) atomicOr(P.status, SV_FLAG_ZERO_RESIDUAL);
+      kind = kTaskBonus;
+      for (int j0 = 0; j0 < nsub; j0 += kSampleUnroll)
+        group_sums<kDtype>(P, t, kind, R, j0, min(nsub, j0 + kSampleUnroll), lane, sub);
+      __syncwarp();
+      __threadfence_block();
+      continue;
+    }
+    const double T = t.u * Rtot;
+    int cand = INT_MAX, last_pos = -1;
+    double pe = 0.0, run = excl;
+    if (in_regs) {
+#pragma unroll
+      for (int u = 0; u < kFinalRegs; ++u) {
+        if (ja + u < jb) {
+          const float sj = v[u];
+          if (sj > 0.f) last_pos = ja + u;
+          if (cand == INT_MAX && run + (double)sj > T) {
+            cand = ja + u;
+            pe = run;
+          }
+          run += (double)sj;
+        }
+      }
+    } else {
+      for (int j = ja; j < jb; ++j) {
+        const float sj = __ldcg(sub + j);
+        if (sj > 0.f) last_pos = j;
+        if (cand == INT_MAX && run + (double)sj > T) {
+          cand = j;
+          pe = run;
+        }
+        run += (double)sj;
+      }
+    }
+    int jstar = warp_min_i(cand);
+    double pexcl;
+    if (jstar != INT_MAX) {
+      const int owner = __ffs(__ballot_sync(0xffffffffu, cand == jstar)) - 1;
+      pexcl = __shfl_sync(0xffffffffu, pe, owner);
+    } else {
+      // u * R at or past the total by rounding: the last sub-chunk with mass.
+      int lp = last_pos;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+      jstar = lp < 0 ? 0 : lp;
+      const float sj = __ldcg(sub + jstar);
+      pexcl = Rtot - (double)sj;
+    }
+    // Prefix sum over the 256 weights of sub-chunk jstar (8 per lane).
+    float r[8];
+    weights8<kDtype>(P, t, kind, R, jstar, lane, r);
+    float pre[8];
+    pre[0] = r[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) pre[k] = pre[k - 1] + r[k];
+    const double incl2 = warp_incl_scan_d((double)pre[7], lane);
+    const double base = pexcl + incl2 - (double)pre[7];
+    const int v0 = jstar * kSubChunk + lane * 8;
+    int c2 = INT_MAX, back = -1;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (c2 == INT_MAX && r[k] > 0.f && base + (double)pre[k] > T) c2 = v0 + k;
+      if (r[k] > 0.f) back = v0 + k;
+    }
+    c2 = warp_min_i(c2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) back = max(back, __shfl_xor_sync(0xffffffffu, back, o));
+    if (lane == 0) {
+      int tok = c2 != INT_MAX ? c2 : (back >= 0 ? back : t.argmax_t);
+      if (tok < 0 || tok >= P.V) tok = t.argmax_t;
+      P.out_tokens[(size_t)b * (P.K + 1) + t.a] = tok;
+    }
+    break;
+  }
+}
+
+}  // namespace sv

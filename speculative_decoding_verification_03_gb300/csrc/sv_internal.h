@@ -10,13 +10,15 @@
 namespace sv {
 
 // ---- row pass geometry -----------------------------------------------------
-constexpr int kStageBytes = 32768;                 // one TMA bulk copy
-constexpr int kStages = 6;                         // ring depth (192 KB in flight per SM)
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumers = kConsumerWarps * 32;    // 512 math threads
-constexpr int kRowThreads = kConsumers + 64;       // + producer warp + epilogue warp
-constexpr int kVecPerStage = kStageBytes / 16;     // 2048 16-byte vectors
-constexpr int kVecPerThread = kVecPerStage / kConsumers;  // 4
+constexpr int kStageBytes = 49152;                 // one TMA bulk copy
+constexpr int kStages = 4;                         // ring depth (192 KB in flight per SM)
+constexpr int kConsumerWarps = 12;
+constexpr int kConsumers = kConsumerWarps * 32;    // 384 math threads
+constexpr int kEpiWarps = 2;                       // epilogue warps (items alternate between them)
+constexpr int kPartSlots = 8;                      // finished items the math warps may run ahead
+constexpr int kRowThreads = kConsumers + 32 + 32 * kEpiWarps;  // + producer warp + epilogue warps
+constexpr int kVecPerStage = kStageBytes / 16;     // 3072 16-byte vectors
+constexpr int kVecPerThread = kVecPerStage / kConsumers;  // 8
 constexpr int kMaxChunks = 16;                     // chunks a row may be split into
 constexpr int kChunkAlignElems = 512;              // chunk starts stay 16-byte aligned within a row
 
@@ -32,6 +34,7 @@ constexpr int kSampleThreads = 256;
 constexpr int kSampleWarps = kSampleThreads / 32;
 constexpr int kSubChunk = 32 * 8;                  // 256 elements per partial sum (one warp, 8 per lane)
 constexpr int kSampleUnroll = 4;                   // sub-chunks a warp loads before reducing
+constexpr int kSampleCtasPerSm = 3;                // grid of the grid-stride sampler
 
 enum TaskKind : int { kTaskNone = 0, kTaskResidual = 1, kTaskBonus = 2 };
 
@@ -49,6 +52,18 @@ struct SampleTask {
   float k0_lo;
   int32_t argmax_t;  // fallback token
   double u;        // U(seed, b, a, 1)
+};
+
+struct SampleParams {
+  const void *target;
+  const void *draft;
+  int B, K, V, esz, dtype;
+  int nsub;       // sub-chunks per row
+  int32_t *out_tokens;
+  uint32_t *status;
+  uint32_t *smp_cnt;  // [B]
+  float *subsum;      // [B][nsub]
+  const SampleTask *tasks;
 };
 
 struct RowPassParams {
@@ -83,25 +98,26 @@ struct RowPassParams {
   sv_row_stats_t *chunk_part;  // [B][2K+1][kMaxChunks]
   SampleTask *tasks;       // [B]
   unsigned long long timeout_ns;
+  // fused sampling: after a sequence's scan, `sp` sample items (b, part) are
+  // published in dq; tickets nstatic .. nstatic + ndyn - 1 take them in order
+  int fused;
+  int sp;        // sample parts per sequence
+  int spc;       // sub-chunks per part
+  int nstatic;   // static row items (= nitems)
+  int ndyn;      // B * sp
+  int *dq;       // [ndyn]: b * sp + part + 1 once published, 0 before
+  uint32_t *dq_tail;   // slots reserved by publishers
+  uint32_t *dq_head;   // slots claimed by producers
+  SampleParams smp;
 };
 
-struct SampleParams {
-  const void *target;
-  const void *draft;
-  int B, K, V, esz, dtype;
-  int nsub;       // sub-chunks per row
-  int per_cta;    // CTAs per sequence
-  int32_t *out_tokens;
-  uint32_t *status;
-  uint32_t *smp_cnt;  // [B]
-  float *subsum;      // [B][nsub]
-  const SampleTask *tasks;
-};
 
 // ---- workspace layout --------------------------------------------------------
+constexpr int kMaxSampleParts = 16;
+
 struct WsLayout {
   size_t counters_off, counters_bytes;  // zeroed by every call
-  size_t ticket_off, row_cnt_off, seq_cnt_off, smp_cnt_off;
+  size_t ticket_off, row_cnt_off, seq_cnt_off, smp_cnt_off, dq_off;
   size_t stats_off, chunk_off, task_off, subsum_off;
   size_t total;
 };
@@ -114,7 +130,7 @@ inline WsLayout ws_layout(int B, int K, int V) {
   const size_t nsub = ((size_t)V + kSubChunk - 1) / kSubChunk;
   size_t off = 256;  // status word and spare header
   L.counters_off = off;
-  L.ticket_off = off;
+  L.ticket_off = off;  // ticket, dq_tail, dq_head
   off += 16;
   L.row_cnt_off = off;
   off += nrow * 4;
@@ -122,6 +138,8 @@ inline WsLayout ws_layout(int B, int K, int V) {
   off += (size_t)B * 4;
   L.smp_cnt_off = off;
   off += (size_t)B * 4;
+  L.dq_off = off;
+  off += (size_t)B * kMaxSampleParts * 4;
   off = align_up(off, 256);
   L.counters_bytes = off - L.counters_off;
   L.stats_off = off;
@@ -137,7 +155,7 @@ inline WsLayout ws_layout(int B, int K, int V) {
 }
 
 // ---- AV refit state ------------------------------------------------------------
-constexpr int kFitSeqPerCta = 128;
+constexpr int kFitSeqPerCta = 64;
 constexpr int kFitMaxCtas = 64;
 constexpr int kFitQ = 6;  // per position: g_w part, H_ww part, g_b, H_wb, H_bb, n
 
@@ -148,9 +166,9 @@ struct AvStateHeader {
   uint32_t K;
 };
 
-// Layout inside the AV state buffer (all doubles):
-//   [header 256 B] [acc: g (K+1), Hww (1), Hwb (K), Hbb (K), n (K)]
-//   [partials: kFitMaxCtas x SV_MAX_K x kFitQ]
+// Layout inside the AV state buffer:
+//   [header 256 B] [acc (doubles): g (K+1), Hww (1), Hwb (K), Hbb (K), n (K)]
+//   [partials (floats): kFitMaxCtas x SV_MAX_K x kFitQ]
 constexpr size_t kAvAccOff = 256;
 constexpr size_t kAvAccDoubles = 4 * SV_MAX_K + 2;
 constexpr size_t kAvPartOff = align_up(kAvAccOff + kAvAccDoubles * 8, 256);
