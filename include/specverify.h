@@ -211,6 +211,28 @@ sv_status_t sv_av_fit_step(int B, int K, float *theta, void *av_state, size_t av
                            const int32_t *kept_len, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sv_verify_fit -- sv_verify and one sv_av_fit_step in a single launch.
+ * Same arguments as sv_verify (theta is required and is updated at the end
+ * of a round), plus the refit state of sv_av_fit_step; kept_len is
+ * draft_len.  Each sequence's acceptance scan adds its labelled drafts'
+ * gradient and Hessian terms (as 2^-32 fixed point, so the sums do not
+ * depend on the order of the additions); the scan that finishes last -- after
+ * every scan has read theta -- performs the round update exactly as
+ * sv_av_fit_step does ("Adaptive Verification without a confidence head",
+ * section "Fitting the coefficients").  The results equal sv_verify followed
+ * by sv_av_fit_step on the same stream up to the rounding of those sums.
+ * ---------------------------------------------------------------------- */
+sv_status_t sv_verify_fit(int B, int K, int V, sv_dtype_t dtype,
+                          const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const int32_t *draft_len,
+                          const float *temperature, uint64_t seed,
+                          float *theta, const sv_row_stats_t *draft_stats,
+                          int32_t *out_tokens, int32_t *out_accept_len,
+                          float *out_feature, float *out_conf,
+                          void *av_state, size_t av_state_bytes, int round_len, float damping_c,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * sv_philox -- the uniform stream itself, for checking: out[b][pos][w] =
  * word w of Philox4x32-10 with key (seed & 0xffffffff, seed >> 32) and
  * counter (b, pos, 0, 0) (Salmon, Moraes, Dror, Shaw, "Parallel Random

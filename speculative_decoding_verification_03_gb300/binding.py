@@ -40,7 +40,8 @@ def build(force: bool = False, nvcc: str = "nvcc") -> str:
     """Compile the CUDA sources for sm_103a into libspecverify.so (in-tree)."""
     csrc = os.path.join(_HERE, "csrc")
     srcs = [os.path.join(csrc, s) for s in _SOURCES]
-    deps = srcs + [os.path.join(csrc, h) for h in ("sv_device.cuh", "sv_internal.h", "sample_common.cuh")] + \
+    deps = srcs + [os.path.join(csrc, h) for h in ("sv_device.cuh", "sv_internal.h", "sample_common.cuh",
+                                                   "avfit_common.cuh")] + \
         [os.path.join(_ROOT, "include", "specverify.h")]
     if not force and os.path.exists(LIB_PATH) and \
             os.path.getmtime(LIB_PATH) >= max(os.path.getmtime(d) for d in deps):
@@ -79,6 +80,8 @@ def lib():
             L.sv_workspace_bytes.restype = SZ
             L.sv_verify.argtypes = [I, I, I, I, P, P, P, P, P, U64, P, P, P, P, P, P, P, SZ, P]
             L.sv_verify.restype = I
+            L.sv_verify_fit.argtypes = [I, I, I, I, P, P, P, P, P, U64, P, P, P, P, P, P, P, SZ, I, F, P, SZ, P]
+            L.sv_verify_fit.restype = I
             L.sv_av_score.argtypes = [I, I, I, I, P, P, P, F, P, P, P, P, P, SZ, P]
             L.sv_av_score.restype = I
             L.sv_av_state_bytes.argtypes = [I]
@@ -146,9 +149,12 @@ def workspace(B: int, K: int, V: int, device="cuda") -> torch.Tensor:
 
 
 def verify(target, draft, draft_tokens, temperature, seed: int, draft_len=None, theta=None, draft_stats=None,
-           want_feature: bool = False, want_conf: bool | None = None, ws=None, out=None, stream=None):
+           want_feature: bool = False, want_conf: bool | None = None, ws=None, out=None, stream=None,
+           av_state: "AVState | None" = None, round_len: int = 1, damping_c: float = 10.0):
     """One verification step on the GPU.  Returns dict(tokens [B][K+1] int32,
-    accept_len [B] int32, feature [B][K] or None, conf [B][K] or None, ws)."""
+    accept_len [B] int32, feature [B][K] or None, conf [B][K] or None, ws).
+    With av_state (and theta) the AV refit step runs in the same launch
+    (sv_verify_fit) and theta is updated in place at the end of a round."""
     B, K1, V = target.shape
     K = K1 - 1
     code = _dtype_code(target)
@@ -170,6 +176,16 @@ def verify(target, draft, draft_tokens, temperature, seed: int, draft_len=None, 
     if ws is None:
         ws = workspace(B, K, V, dev)
     out["ws"] = ws
+    if av_state is not None:
+        if theta is None:
+            raise ValueError("the fused refit needs theta")
+        rc = lib().sv_verify_fit(B, K, V, code, _ptr(target), _ptr(draft), _ptr(draft_tokens), _ptr(draft_len),
+                                 _ptr(temperature), ctypes.c_uint64(int(seed) & (2**64 - 1)), _ptr(theta),
+                                 _ptr(draft_stats), _ptr(out["tokens"]), _ptr(out["accept_len"]),
+                                 _ptr(out["feature"]), _ptr(out["conf"]), _ptr(av_state.buf), av_state.buf.numel(),
+                                 int(round_len), float(damping_c), _ptr(ws), ws.numel(), _stream(stream))
+        _check(rc, "sv_verify_fit")
+        return out
     rc = lib().sv_verify(B, K, V, code, _ptr(target), _ptr(draft), _ptr(draft_tokens), _ptr(draft_len),
                          _ptr(temperature), ctypes.c_uint64(int(seed) & (2**64 - 1)), _ptr(theta),
                          _ptr(draft_stats), _ptr(out["tokens"]), _ptr(out["accept_len"]), _ptr(out["feature"]),
@@ -230,9 +246,10 @@ class AVState:
 class HostSession:
     """Verification from host buffers: each step copies the inputs from
     (pinned) host tensors into device buffers allocated once, runs
-    sv_verify and sv_av_fit_step, and copies the emitted tokens and accept
-    lengths back into host tensors.  All on one stream, no synchronisation:
-    the host outputs are valid after the stream is synchronised."""
+    sv_verify_fit (verification and the refit step in one launch), and copies
+    the emitted tokens and accept lengths back into host tensors.  All on one
+    stream, no synchronisation: the host outputs are valid after the stream
+    is synchronised."""
 
     def __init__(self, B, K, V, dtype, device, theta0, round_len=1, damping_c=10.0):
         self.B, self.K, self.V = B, K, V
@@ -254,9 +271,8 @@ class HostSession:
         for name in ("target", "draft", "draft_tokens", "temperature"):
             getattr(self, name).copy_(host[name], non_blocking=True)
         verify(self.target, self.draft, self.draft_tokens, self.temperature, seed, theta=self.theta,
-               want_feature=True, ws=self.ws, out=self.out)
-        self.state.fit_step(self.theta, self.out["feature"], self.out["accept_len"], round_len=self.round_len,
-                            damping_c=self.damping_c)
+               want_feature=True, ws=self.ws, out=self.out, av_state=self.state, round_len=self.round_len,
+               damping_c=self.damping_c)
         tokens_out.copy_(self.out["tokens"], non_blocking=True)
         accept_out.copy_(self.out["accept_len"], non_blocking=True)
 

@@ -111,11 +111,23 @@ size_t sv_workspace_bytes(int B, int K, int V) {
   return ws_layout(B, K, V).total;
 }
 
-sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype, const void *target_logits, const void *draft_logits,
-                      const int32_t *draft_tokens, const int32_t *draft_len, const float *temperature, uint64_t seed,
-                      const float *theta, const sv_row_stats_t *draft_stats, int32_t *out_tokens,
-                      int32_t *out_accept_len, float *out_feature, float *out_conf, void *workspace,
-                      size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+struct FitArgs {
+  float *theta;
+  void *av_state;
+  size_t av_state_bytes;
+  int round_len;
+  float damping_c;
+};
+
+sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *target_logits, const void *draft_logits,
+                        const int32_t *draft_tokens, const int32_t *draft_len, const float *temperature,
+                        uint64_t seed, const float *theta, const sv_row_stats_t *draft_stats, int32_t *out_tokens,
+                        int32_t *out_accept_len, float *out_feature, float *out_conf, void *workspace,
+                        size_t workspace_bytes, void *stream, const FitArgs *fit) {
   if (!shape_ok(B, K, V) || (dtype != SV_BF16 && dtype != SV_FP32)) return SV_ERR_INVALID;
   if (B == 0) return SV_OK;
   const int esz = esize(dtype);
@@ -134,7 +146,7 @@ sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype, const void *target_
   if (ds != SV_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  RowPassParams P;
+  RowPassParams P{};
   std::memset(&P, 0, sizeof P);
   P.target = target_logits;
   P.draft = draft_logits;
@@ -158,9 +170,18 @@ sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype, const void *target_
   P.out_feature = out_feature;
   P.out_conf = out_conf;
   fill_ws(P, workspace, L);
+  if (fit) {
+    P.fit = 1;
+    P.round_len = fit->round_len;
+    P.damping_c = fit->damping_c;
+    P.theta_rw = fit->theta;
+    P.av_state = static_cast<unsigned char *>(fit->av_state);
+    P.fitacc = reinterpret_cast<unsigned long long *>(static_cast<unsigned char *>(workspace) + L.fitacc_off);
+    P.scans_done = P.ticket + 3;
+  }
 
   unsigned char *w = static_cast<unsigned char *>(workspace);
-  SampleParams S;
+  SampleParams S{};
   std::memset(&S, 0, sizeof S);
   S.target = target_logits;
   S.draft = draft_logits;
@@ -210,6 +231,38 @@ sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype, const void *target_
   return cuda_status(e);
 }
 
+}  // namespace
+
+extern "C" {
+
+sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype, const void *target_logits, const void *draft_logits,
+                      const int32_t *draft_tokens, const int32_t *draft_len, const float *temperature, uint64_t seed,
+                      const float *theta, const sv_row_stats_t *draft_stats, int32_t *out_tokens,
+                      int32_t *out_accept_len, float *out_feature, float *out_conf, void *workspace,
+                      size_t workspace_bytes, void *stream) {
+  return verify_impl(B, K, V, dtype, target_logits, draft_logits, draft_tokens, draft_len, temperature, seed, theta,
+                     draft_stats, out_tokens, out_accept_len, out_feature, out_conf, workspace, workspace_bytes,
+                     stream, nullptr);
+}
+
+sv_status_t sv_verify_fit(int B, int K, int V, sv_dtype_t dtype, const void *target_logits, const void *draft_logits,
+                          const int32_t *draft_tokens, const int32_t *draft_len, const float *temperature,
+                          uint64_t seed, float *theta, const sv_row_stats_t *draft_stats, int32_t *out_tokens,
+                          int32_t *out_accept_len, float *out_feature, float *out_conf, void *av_state,
+                          size_t av_state_bytes, int round_len, float damping_c, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+  if (!theta || !aligned(theta, 4) || round_len < 1 || !(damping_c >= 0.f)) return SV_ERR_INVALID;
+  if (K < 0 || K > SV_MAX_K) return SV_ERR_INVALID;
+  if (!av_state || !aligned(av_state, 256) || av_state_bytes < sv_av_state_bytes(K)) return SV_ERR_WORKSPACE;
+  if (B == 0)  // no sequences: the round still advances by one step
+    return sv_av_fit_step(0, K, theta, av_state, av_state_bytes, round_len, damping_c, nullptr, nullptr, nullptr,
+                          stream);
+  FitArgs f{theta, av_state, av_state_bytes, round_len, damping_c};
+  return verify_impl(B, K, V, dtype, target_logits, draft_logits, draft_tokens, draft_len, temperature, seed, theta,
+                     draft_stats, out_tokens, out_accept_len, out_feature, out_conf, workspace, workspace_bytes,
+                     stream, &f);
+}
+
 sv_status_t sv_av_score(int B, int K, int V, sv_dtype_t dtype, const void *draft_logits, const float *temperature,
                         const float *theta, float keep_threshold, float *out_feature, float *out_conf,
                         int32_t *out_kept_len, sv_row_stats_t *out_draft_stats, void *workspace,
@@ -233,7 +286,7 @@ sv_status_t sv_av_score(int B, int K, int V, sv_dtype_t dtype, const void *draft
     if (out_kept_len) return cuda_status(cudaMemsetAsync(out_kept_len, 0, (size_t)B * 4, st));
     return SV_OK;
   }
-  RowPassParams P;
+  RowPassParams P{};
   std::memset(&P, 0, sizeof P);
   P.draft = draft_logits;
   P.temperature = temperature;
@@ -283,7 +336,7 @@ sv_status_t sv_av_fit_step(int B, int K, float *theta, void *av_state, size_t av
   int sms = 0;
   const sv_status_t ds = device_info(&sms);
   if (ds != SV_OK) return ds;
-  FitParams F;
+  FitParams F{};
   F.B = B;
   F.K = K;
   F.round_len = round_len;

@@ -20,6 +20,7 @@
 // adds them in CTA order (deterministic), lane i owning position i, updates
 // the fp64 round accumulators and, at the end of the round, solves with warp
 // reductions for the Schur terms and writes theta.
+#include "avfit_common.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -32,7 +33,6 @@ __global__ void avfit_kernel(const FitParams P) {
   const int K = P.K;
   const int G = gridDim.x;
   AvStateHeader *hdr = reinterpret_cast<AvStateHeader *>(P.state);
-  double *acc = reinterpret_cast<double *>(P.state + kAvAccOff);
   float *parts = reinterpret_cast<float *>(P.state + kAvPartOff);
   __shared__ int s_last;
 
@@ -84,69 +84,15 @@ __global__ void avfit_kernel(const FitParams P) {
   __threadfence();
 
   // Last CTA, warp 0, lane i = position i: add the CTA partials (in CTA
-  // order) to the round accumulators, acc = [g (K+1; g[0] = slope), Hww,
-  // Hwb[K], Hbb[K], n[K]].
-  double *g = acc;
-  double *Hww = acc + (K + 1);
-  double *Hwb = Hww + 1;
-  double *Hbb = Hwb + K;
-  double *n = Hbb + K;
+  // order) and update the round.
   double t[kFitQ] = {0, 0, 0, 0, 0, 0};
   if (lane < K) {
     for (int c = 0; c < G; ++c)
 #pragma unroll
       for (int j = 0; j < kFitQ; ++j) t[j] += (double)__ldcg(parts + ((size_t)c * SV_MAX_K + lane) * kFitQ + j);
   }
-  double gb = 0, hwb = 0, hbb = 0, nn = 0;
-  if (lane < K) {
-    gb = __ldcg(g + 1 + lane) + t[2];
-    hwb = __ldcg(Hwb + lane) + t[3];
-    hbb = __ldcg(Hbb + lane) + t[4];
-    nn = __ldcg(n + lane) + t[5];
-  }
-  const double gw = __ldcg(g) + warp_sum_d(t[0]);
-  const double hww = __ldcg(Hww) + warp_sum_d(t[1]);
-  const uint32_t step = hdr->step + 1u;
-  bool solved = false;
-  if ((int)step >= P.round_len) {
-    // End of round: damped Newton step over omega and the labelled intercepts
-    // (Schur complement of the arrow-shaped Hessian on omega).
-    const double ntot = warp_sum_d(nn);
-    const double trace = hww + warp_sum_d(hbb);
-    if (ntot > 0.0) {
-      const double ridge = 1e-9 * trace / (double)(K + 1);
-      const bool has = lane < K && nn > 0.0;
-      const double d = hbb + ridge;
-      const double s1 = warp_sum_d(has ? hwb * hwb / d : 0.0);
-      const double s2 = warp_sum_d(has ? hwb * gb / d : 0.0);
-      const double a = hww + ridge - s1, rhs = gw - s2;
-      if (a > 0.0 && isfinite(rhs)) {
-        const double dw = rhs / a;
-        const double c = (double)P.damping_c;
-        if (lane == 0) P.theta[0] = (float)((double)P.theta[0] - ntot / (ntot + c) * dw);
-        if (has) {
-          const double db = (gb - hwb * dw) / d;
-          P.theta[1 + lane] = (float)((double)P.theta[1 + lane] - nn / (nn + c) * db);
-        }
-      } else if (lane == 0) {
-        atomicOr(&hdr->status, SV_FLAG_FIT_SINGULAR);
-      }
-    }
-    solved = true;
-  }
-  // write the accumulators back (cleared at the end of a round)
-  if (lane < K) {
-    g[1 + lane] = solved ? 0.0 : gb;
-    Hwb[lane] = solved ? 0.0 : hwb;
-    Hbb[lane] = solved ? 0.0 : hbb;
-    n[lane] = solved ? 0.0 : nn;
-  }
-  if (lane == 0) {
-    g[0] = solved ? 0.0 : gw;
-    *Hww = solved ? 0.0 : hww;
-    hdr->step = solved ? 0u : step;
-    hdr->cta_done = 0u;
-  }
+  av_round_update(P.state, P.theta, K, P.round_len, P.damping_c, t, lane);
+  if (lane == 0) hdr->cta_done = 0u;
 }
 
 __global__ void philox_kernel(uint64_t seed, int nb, int npos, uint32_t *out) {

@@ -26,6 +26,7 @@
 #include <cfloat>
 #include <climits>
 
+#include "avfit_common.cuh"
 #include "sample_common.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
@@ -119,6 +120,7 @@ struct __align__(128) Smem {
   uint64_t pfull[kPartSlots];
   uint64_t pempty[kPartSlots];
   int abort_flag;
+  int epi_next;  // next partial item for the epilogue warps
 };
 
 __device__ __forceinline__ int kept_len_of(const RowPassParams &P, int b) {
@@ -132,14 +134,19 @@ __device__ __forceinline__ float row_scale(const RowPassParams &P, int b) {
   return tau > 0.f ? kLog2e / tau : kLog2e;  // greedy (and invalid) rows at tau = 1
 }
 
-// Slot -> (is_target, position) for the streaming mode.
-__device__ __forceinline__ void slot_kind(int mode, int slot, int &is_target, int &pos) {
+// Slot -> (is_target, position) for the streaming mode.  Verify modes stream a
+// sequence's rows from the highest position down: the rows a residual or a
+// bonus re-reads are most often the low positions (a rejection at position i
+// needs the first i drafts accepted), so those are read last and are still
+// in L2 when the sequence completes.
+__device__ __forceinline__ void slot_kind(int mode, int K, int slot, int &is_target, int &pos) {
   if (mode == kVerifyFull) {
+    // slots: tK, d(K-1), t(K-1), ..., d0, t0
     is_target = !(slot & 1);
-    pos = slot >> 1;
+    pos = K - ((slot + 1) >> 1);
   } else if (mode == kVerifyTargets) {
     is_target = 1;
-    pos = slot;
+    pos = K - slot;
   } else {
     is_target = 0;
     pos = slot;
@@ -406,13 +413,50 @@ __device__ __forceinline__ void consume_scalar(WarpState &s, float v, int idx, i
 // ---------------------------------------------------------------------------
 // Per-sequence completion (epilogue warp, all 32 lanes).
 // ---------------------------------------------------------------------------
+// q * 2^32 rounded to the nearest integer (ties away from zero), by integer
+// operations on the fp32 encoding; |q| < 2^30.  The fused refit's sums are
+// exact in this fixed point, so they do not depend on the order of the adds.
+__device__ __forceinline__ long long fixed_2p32(float q) {
+  const uint32_t bits = __float_as_uint(q);
+  const int e = (int)((bits >> 23) & 0xffu);
+  if (e == 0 || e == 0xff) return 0;  // zero, subnormal (< 2^-126) or not finite
+  const long long m = (long long)((bits & 0x7fffffu) | 0x800000u);
+  const int sh = e - 118;  // q * 2^32 = m * 2^(e - 150 + 32)
+  long long v;
+  if (sh >= 0) v = m << (sh < 38 ? sh : 38);
+  else if (sh > -26) v = (m + (1ll << (-sh - 1))) >> (-sh);
+  else v = 0;
+  return (bits >> 31) ? -v : v;
+}
+
+// Acceptance test u < p(d)/q(d) at one position, in fp64 ("Accelerating
+// Large Language Model Decoding with Speculative Sampling", Algorithm 2):
+// ln p(d) = (z_t(d) - m_t) / tau - ln S_t and likewise for q.  The fp32 fast
+// path below defers to this one whenever it is not certain.
+__device__ __forceinline__ bool reject_fp64(float zt, float zd, const Part &T, const Part &D, double invtau,
+                                            double u) {
+  const double lnSt = log1p((double)T.E), lnSd = log1p((double)D.E);
+  const double lq = ((double)zd - (double)D.m) * invtau - lnSd;
+  double ratio;
+  if (lq == -INFINITY) {
+    ratio = INFINITY;
+  } else {
+    const double lp = ((double)zt - (double)T.m) * invtau - lnSt;
+    ratio = exp(lp - lq);
+  }
+  return !(u < ratio);
+}
+
 __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
   const int K = P.K;
   const int k = kept_len_of(P, b);
   const float tau_f = __ldg(P.temperature + b);
   const bool bad_tau = !(tau_f >= 0.f);
   const bool greedy = !(tau_f > 0.f);
-  const double invtau = greedy ? 1.0 : 1.0 / (double)tau_f;
+  // fp32 1/tau and log2(e)/tau, both correctly rounded (the row pass uses the
+  // same scale for its statistics)
+  const float inv_f = greedy ? 1.f : 1.f / tau_f;
+  const float c_f = greedy ? kLog2e : kLog2e / tau_f;
   const size_t rowb = (size_t)P.V;
   uint32_t flags = 0;
   if (lane == 0) {
@@ -424,11 +468,14 @@ __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
   }
   const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
 
-  // Lane i <= k: ln S of target row i; lane i < k: ln S of draft row i, the
-  // acceptance test at position i, the AV feature and confidence.
-  bool reject = false;
+  // Lane i <= k: statistics of target row i; lane i < k: those of draft row
+  // i and the acceptance test at position i.  The test runs in fp32 and is
+  // kept when |ln u - ln(p/q)| exceeds a bound on its rounding error (a few
+  // fp32 ulps of each term); otherwise the warp redoes it in fp64.
+  bool reject = false, unsure = false, in_range = false;
   int d = -1;
-  double lnSt = 0.0, lnSd = 0.0;
+  float u = 0.f, zt = 0.f, zd = 0.f;
+  float lnSt = 0.f;
   Part T, D;
   T.m = D.m = 0.f;
   T.E = D.E = 0.f;
@@ -436,86 +483,73 @@ __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
   T.flags = D.flags = 0u;
   if (lane <= k) {
     T = load_stats_cg(st + 2 * lane);
-    lnSt = log1p((double)T.E);
+    lnSt = log1pf(T.E);
     flags |= T.flags & SV_FLAG_NONFINITE;
   }
   if (lane < k) {
     const int i = lane;
     D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + i) : load_stats_cg(st + 2 * i + 1);
-    lnSd = log1p((double)D.E);
     flags |= D.flags & SV_FLAG_NONFINITE;
     d = __ldg(P.draft_tokens + (size_t)b * K + i);
-    const bool in_range = d >= 0 && d < P.V;
+    in_range = d >= 0 && d < P.V;
     if (!in_range) flags |= SV_FLAG_TOKEN_RANGE;
     if (greedy) {
       reject = !(in_range && d == T.arg);
     } else {
-      const double u = uniform24(P.seed, (uint32_t)b, (uint32_t)i, 0);
-      double ratio = 0.0;
+      u = uniform24f(P.seed, (uint32_t)b, (uint32_t)i, 0);
+      reject = true;  // p/q = 0 for an out-of-range token
       if (in_range) {
         const long long trow = ((long long)b * (K + 1) + i) * (long long)rowb;
         const long long drow = ((long long)b * K + i) * (long long)rowb;
-        const double zt = (double)logit_at(P.target, P.dtype, trow + d);
-        const double zd = (double)logit_at(P.draft, P.dtype, drow + d);
-        const double lq = (zd - (double)D.m) * invtau - lnSd;
-        if (lq == -INFINITY) {
-          ratio = INFINITY;
-        } else {
-          const double lp = (zt - (double)T.m) * invtau - lnSt;
-          ratio = exp(lp - lq);
-        }
-      }
-      reject = !(u < ratio);
-    }
-    if (P.out_feature || P.out_conf) {
-      const double E = (double)D.E;
-      double x = E > 0.0 ? -log(E) : 30.0;
-      x = x > 30.0 ? 30.0 : (x < -30.0 ? -30.0 : x);
-      if (P.out_feature) P.out_feature[(size_t)b * K + i] = (float)x;
-      if (P.out_conf) {
-        const double z = (double)__ldg(P.theta) * x + (double)__ldg(P.theta + 1 + i);
-        P.out_conf[(size_t)b * K + i] = (float)(1.0 / (1.0 + exp(-z)));
+        zt = logit_at(P.target, P.dtype, trow + d);
+        zd = logit_at(P.draft, P.dtype, drow + d);
+        const float lnSd = log1pf(D.E);
+        const float A = (zt - T.m) * inv_f, Bq = (zd - D.m) * inv_f;
+        const float dl = (A - lnSt) - (Bq - lnSd);  // ln(p/q)
+        const float lu = logf(u);
+        const float band = 2e-6f + 4e-7f * (fabsf(A) + fabsf(Bq) + lnSt + lnSd + fabsf(lu));
+        unsure = u == 0.f || !(fabsf(dl - lu) > band);  // also NaN
+        reject = !(lu < dl);
       }
     }
-  } else if (lane < K) {
-    if (P.out_feature) P.out_feature[(size_t)b * K + lane] = __int_as_float(0x7fc00000);
-    if (P.out_conf) P.out_conf[(size_t)b * K + lane] = __int_as_float(0x7fc00000);
+  }
+  if (__any_sync(0xffffffffu, unsure)) {
+    if (lane < k && !greedy && in_range) reject = reject_fp64(zt, zd, T, D, 1.0 / (double)tau_f, (double)u);
   }
   const unsigned rej = __ballot_sync(0xffffffffu, reject);
   const int a = rej ? (__ffs(rej) - 1) : k;
 
   // Row a's statistics from lane a.
   const float Ta_m = __shfl_sync(0xffffffffu, T.m, a);
+  const float Ta_E = __shfl_sync(0xffffffffu, T.E, a);
   const int Ta_arg = __shfl_sync(0xffffffffu, T.arg, a);
-  const double lnSt_a = __shfl_sync(0xffffffffu, lnSt, a);
+  const float lnSt_a = __shfl_sync(0xffffffffu, lnSt, a);
   const float Da_m = __shfl_sync(0xffffffffu, D.m, a);
-  const double lnSd_a = __shfl_sync(0xffffffffu, lnSd, a);
+  const float Da_E = __shfl_sync(0xffffffffu, D.E, a);
 
-  // Emitted tokens: accepted drafts, the position-a token (written here for
-  // greedy rows, by the sampler otherwise), then -1.
-  if (lane <= K) {
-    int32_t v = -1;
-    if (lane < a) v = d;
-    else if (lane == a && greedy) v = (Ta_arg >= 0 && Ta_arg < P.V) ? Ta_arg : 0;
-    P.out_tokens[(size_t)b * (K + 1) + lane] = v;
-  }
+  // The sample task first (the sampler waits for it), then the outputs.
   if (lane == 0) {
-    P.out_accept_len[b] = a;
     SampleTask t;
     t.kind = greedy ? kTaskNone : (a < k ? kTaskResidual : kTaskBonus);
     t.a = a;
     t.argmax_t = (Ta_arg >= 0 && Ta_arg < P.V) ? Ta_arg : 0;
-    t.c = (float)(kLog2ed * invtau);
-    t.invtau = (float)invtau;
-    t.nbt = (float)(-((double)Ta_m * (kLog2ed * invtau) + lnSt_a * kLog2ed));
+    t.c = c_f;
+    t.invtau = inv_f;
+    // p(v) = 2^(z(v) c + nbt): an overall scale of the weights, which the
+    // draw does not depend on, so fp32 suffices
+    t.nbt = -fmaf(Ta_m, c_f, lnSt_a * kLog2e);
     t.k0_hi = 0.f;
     t.k0_lo = 0.f;
     if (t.kind == kTaskResidual) {
-      const double k0 = ((double)Ta_m - (double)Da_m) * invtau + lnSt_a - lnSd_a;
+      // q(v)/p(v) = exp((z_d(v) - z_t(v)) / tau + k0); k0 sets where the
+      // residual p - q changes sign and is kept to fp64 precision:
+      // k0 = (m_t - m_d) / tau + ln(S_t / S_d), S = 1 + E
+      const double lnr = log1p(((double)Ta_E - (double)Da_E) / (1.0 + (double)Da_E));
+      const double k0 = ((double)Ta_m - (double)Da_m) / (double)tau_f + lnr;
       t.k0_hi = (float)k0;
       t.k0_lo = (float)(k0 - (double)t.k0_hi);
     }
-    t.u = greedy ? 0.0 : uniform24(P.seed, (uint32_t)b, (uint32_t)a, 1);
+    t.u = greedy ? 0.0 : (double)uniform24f(P.seed, (uint32_t)b, (uint32_t)a, 1);
     P.tasks[b] = t;
     if (P.fused) {
       // hand the sequence's sample items to the producers (all sp of them,
@@ -525,9 +559,69 @@ __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
       const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)P.sp);
       for (int q = 0; q < P.sp; ++q) st_relaxed_gpu(P.dq + base + q, b * P.sp + q + 1);
     }
+    P.out_accept_len[b] = a;
+  }
+
+  // Emitted tokens: accepted drafts, the position-a token (written here for
+  // greedy rows, by the sampler otherwise), then -1.
+  if (lane <= K) {
+    int32_t v = -1;
+    if (lane < a) v = d;
+    else if (lane == a && greedy) v = (Ta_arg >= 0 && Ta_arg < P.V) ? Ta_arg : 0;
+    P.out_tokens[(size_t)b * (K + 1) + lane] = v;
+  }
+
+  // AV feature x = -ln E = logit(q_max) of the draft row and the confidence
+  // sigmoid(omega x + beta_i) ("Adaptive Verification without a confidence
+  // head"), fp32; theta through L2 (the fused refit rewrites it).
+  // (theta may be null when only features are asked for; the fused refit
+  // and out_conf require it)
+  float x = 0.f, conf = 0.f;
+  if (lane < k && (P.out_feature || P.out_conf || P.fit)) {
+    x = D.E > 0.f ? -logf(D.E) : 30.f;
+    x = x > 30.f ? 30.f : (x < -30.f ? -30.f : x);
+    if (P.theta) conf = 1.0f / (1.0f + expf(-fmaf(__ldcg(P.theta), x, __ldcg(P.theta + 1 + lane))));
+  }
+  if (lane < K) {
+    const float nan = __int_as_float(0x7fc00000);
+    if (P.out_feature) P.out_feature[(size_t)b * K + lane] = lane < k ? x : nan;
+    if (P.out_conf) P.out_conf[(size_t)b * K + lane] = lane < k ? conf : nan;
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0 && flags) atomicOr(P.status, flags);
+
+  if (P.fit) {
+    // Fused refit: this sequence's labelled drafts (up to and including the
+    // first rejection) add their log-loss gradient and Hessian terms
+    // ("Fitting the coefficients").
+    const int nlab = min(a + 1, k);
+    if (lane < nlab) {
+      const float y = lane < a ? 1.0f : 0.0f;
+      const float r = conf - y, w = conf * (1.0f - conf);
+      const float q[kFitQ] = {r * x, w * x * x, r, w * x, w, 1.0f};
+#pragma unroll
+      for (int j = 0; j < kFitQ; ++j)
+        atomicAdd(P.fitacc + lane * kFitQ + j, (unsigned long long)fixed_2p32(q[j]));
+    }
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence();
+      last = atomicAdd(P.scans_done, 1u) == (uint32_t)P.B - 1u;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      // every scan has read theta: the round update may now change it
+      __threadfence();
+      double t[kFitQ] = {0, 0, 0, 0, 0, 0};
+      if (lane < K) {
+#pragma unroll
+        for (int j = 0; j < kFitQ; ++j)
+          t[j] = (double)(long long)__ldcg(P.fitacc + lane * kFitQ + j) * (1.0 / kFitFixedScale);
+      }
+      av_round_update(P.av_state, P.theta_rw, K, P.round_len, P.damping_c, t, lane);
+    }
+  }
 }
 
 __device__ void finish_score(const RowPassParams &P, int b, int lane) {
@@ -589,6 +683,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
       mbar_init(&S.pempty[s], 1);
     }
     S.abort_flag = 0;
+    S.epi_next = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -737,7 +832,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
         cached_c = row_scale(P, b);
       }
       int is_target, pos;
-      slot_kind(P.mode, slot, is_target, pos);
+      slot_kind(P.mode, K, slot, is_target, pos);
       if (P.mode != kScore) {
         if (is_target ? (pos > cached_k) : (pos >= cached_k)) continue;
       }
@@ -825,9 +920,16 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
   if (warp >= kEpilogueWarp0) {
     // ------------------------------------------------------------------ epilogue
     const int K = P.K;
-    // items alternate between the epilogue warps: this one takes items
-    // n = e, e + kEpiWarps, ... in slots n % kPartSlots
-    for (int it = warp - kEpilogueWarp0;; it += kEpiWarps) {
+    // Each epilogue warp takes the next item n (slot n % kPartSlots) from a
+    // shared counter, so a warp busy with a sequence's scan or draw does not
+    // hold up the items behind it.  Items are produced in order and a slot
+    // is refilled only after its item was read, so the parity of n / kPartSlots
+    // names the right phase of the slot's barrier.  Every warp leaves on the
+    // first end-of-work marker it takes; there is one marker per warp.
+    for (;;) {
+      int it = 0;
+      if (lane == 0) it = atomicAdd(&S.epi_next, 1);
+      it = __shfl_sync(0xffffffffu, it, 0);
       const int slot = it % kPartSlots;
       if (!mbar_wait_bounded(&S.pfull[slot], (uint32_t)((it / kPartSlots) & 1), abort_flag, P.status, P.timeout_ns)) break;
       const PartInfo info = S.pinfo[slot];

@@ -127,11 +127,56 @@ __device__ __forceinline__ float sum8(const float (&r)[8]) {
   return ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
 }
 
-__device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
+// Double-float numbers: an unevaluated sum hi + lo of two fp32 values, about
+// 48 bits of significand (Dekker, "A floating-point technique for extending
+// the available precision", 1971; Knuth's two-sum).  Used for the prefix sums
+// of the draw, where fp64 would run at a small fraction of the fp32 rate on
+// this GPU.  __fadd_rn keeps the compiler from reassociating the error terms.
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fadd_rn(s, -a);
+  const float e = __fadd_rn(__fadd_rn(a, -__fadd_rn(s, -bb)), __fadd_rn(b, -bb));
+  return {s, e};
+}
+
+__device__ __forceinline__ DF fast_two_sum(float a, float b) {  // |a| >= |b| or a == 0
+  const float s = __fadd_rn(a, b);
+  return {s, __fadd_rn(b, -__fadd_rn(s, -a))};
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = two_sum(a.hi, b.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ DF df_add_f(DF a, float b) {
+  const DF s = two_sum(a.hi, b);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, a.lo));
+}
+
+// a > b, decided on the double-float values
+__device__ __forceinline__ bool df_gt(DF a, DF b) {
+  return __fadd_rn(__fadd_rn(a.hi, -b.hi), __fadd_rn(a.lo, -b.lo)) > 0.f;
+}
+
+// u * R for an fp32 u, as a double-float (the product's error by an FMA)
+__device__ __forceinline__ DF df_scale(float u, DF r) {
+  const float p = __fmul_rn(u, r.hi);
+  const float e = __fmaf_rn(u, r.hi, -p);
+  return fast_two_sum(p, __fmaf_rn(u, r.lo, e));
+}
+
+__device__ __forceinline__ DF warp_incl_scan_df(DF v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
+    DF n;
+    n.hi = __shfl_up_sync(0xffffffffu, v.hi, o);
+    n.lo = __shfl_up_sync(0xffffffffu, v.lo, o);
+    if (lane >= o) v = df_add(v, n);
   }
   return v;
 }
@@ -172,9 +217,9 @@ __device__ __forceinline__ void group_sums(const SampleParams &P, const SampleTa
 
 // One warp locates the token of sequence b from its sub-chunk sums.  Lane l
 // owns sub-chunks [l q, l q + q); when q <= kFinalRegs they are read once into
-// registers.  Prefix sums across sub-chunks are fp64 (a prefix error of
-// 1e-7 R would move the crossing at large V); inside the crossing sub-chunk
-// the prefix is fp32 from the sub-chunk's start.
+// registers.  Prefix sums across sub-chunks are double-float (a prefix error
+// of 1e-7 R would move the crossing at large V); inside the crossing
+// sub-chunk the prefix is fp32 from the lane's start.
 constexpr int kFinalRegs = 24;
 
 template <int kDtype>
@@ -184,22 +229,24 @@ __device__ void finalize_warp(const SampleParams &P, const SampleTask &t, int b,
   const int q = (nsub + 31) / 32;
   const int ja = min(nsub, lane * q), jb = min(nsub, ja + q);
   const bool in_regs = q <= kFinalRegs;
+  const float u = (float)t.u;  // 24-bit uniform: exact
   int kind = t.kind;
   for (int attempt = 0; attempt < 2; ++attempt) {
     float v[kFinalRegs];
-    double mine = 0.0;
+    DF mine = {0.f, 0.f};
     if (in_regs) {
 #pragma unroll
-      for (int u = 0; u < kFinalRegs; ++u) v[u] = (ja + u < jb) ? __ldcg(sub + ja + u) : 0.f;
+      for (int k = 0; k < kFinalRegs; ++k) v[k] = (ja + k < jb) ? __ldcg(sub + ja + k) : 0.f;
 #pragma unroll
-      for (int u = 0; u < kFinalRegs; ++u) mine += (double)v[u];
+      for (int k = 0; k < kFinalRegs; ++k) mine = df_add_f(mine, v[k]);
     } else {
-      for (int j = ja; j < jb; ++j) mine += (double)__ldcg(sub + j);
+      for (int j = ja; j < jb; ++j) mine = df_add_f(mine, __ldcg(sub + j));
     }
-    const double incl = warp_incl_scan_d(mine, lane);
-    const double Rtot = __shfl_sync(0xffffffffu, incl, 31);
-    const double excl = incl - mine;
-    if (!(Rtot > 0.0) && kind == kTaskResidual && attempt == 0) {
+    const DF incl = warp_incl_scan_df(mine, lane);
+    DF Rtot;
+    Rtot.hi = __shfl_sync(0xffffffffu, incl.hi, 31);
+    Rtot.lo = __shfl_sync(0xffffffffu, incl.lo, 31);
+    if (!(Rtot.hi > 0.f) && kind == kTaskResidual && attempt == 0) {
       // Zero residual mass (rounding only): sample p_a instead, and say so.
       if (lane == 0) atomicOr(P.status, SV_FLAG_ZERO_RESIDUAL);
       kind = kTaskBonus;
@@ -209,46 +256,50 @@ __device__ void finalize_warp(const SampleParams &P, const SampleTask &t, int b,
       __threadfence_block();
       continue;
     }
-    const double T = t.u * Rtot;
+    const DF T = df_scale(u, Rtot);
+    // the crossing sub-chunk: the first j with prefix(j) + s_j > T
     int cand = INT_MAX, last_pos = -1;
-    double pe = 0.0, run = excl;
+    DF pe = {0.f, 0.f};
+    DF run = df_add(incl, {-mine.hi, -mine.lo});  // exclusive prefix of this lane
     if (in_regs) {
 #pragma unroll
-      for (int u = 0; u < kFinalRegs; ++u) {
-        if (ja + u < jb) {
-          const float sj = v[u];
-          if (sj > 0.f) last_pos = ja + u;
-          if (cand == INT_MAX && run + (double)sj > T) {
-            cand = ja + u;
+      for (int k = 0; k < kFinalRegs; ++k) {
+        if (ja + k < jb) {
+          const float sj = v[k];
+          if (sj > 0.f) last_pos = ja + k;
+          const DF nxt = df_add_f(run, sj);
+          if (cand == INT_MAX && df_gt(nxt, T)) {
+            cand = ja + k;
             pe = run;
           }
-          run += (double)sj;
+          run = nxt;
         }
       }
     } else {
       for (int j = ja; j < jb; ++j) {
         const float sj = __ldcg(sub + j);
         if (sj > 0.f) last_pos = j;
-        if (cand == INT_MAX && run + (double)sj > T) {
+        const DF nxt = df_add_f(run, sj);
+        if (cand == INT_MAX && df_gt(nxt, T)) {
           cand = j;
           pe = run;
         }
-        run += (double)sj;
+        run = nxt;
       }
     }
     int jstar = warp_min_i(cand);
-    double pexcl;
+    DF pexcl;
     if (jstar != INT_MAX) {
       const int owner = __ffs(__ballot_sync(0xffffffffu, cand == jstar)) - 1;
-      pexcl = __shfl_sync(0xffffffffu, pe, owner);
+      pexcl.hi = __shfl_sync(0xffffffffu, pe.hi, owner);
+      pexcl.lo = __shfl_sync(0xffffffffu, pe.lo, owner);
     } else {
       // u * R at or past the total by rounding: the last sub-chunk with mass.
       int lp = last_pos;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
       jstar = lp < 0 ? 0 : lp;
-      const float sj = __ldcg(sub + jstar);
-      pexcl = Rtot - (double)sj;
+      pexcl = df_add_f(Rtot, -__ldcg(sub + jstar));
     }
     // Prefix sum over the 256 weights of sub-chunk jstar (8 per lane).
     float r[8];
@@ -257,13 +308,13 @@ __device__ void finalize_warp(const SampleParams &P, const SampleTask &t, int b,
     pre[0] = r[0];
 #pragma unroll
     for (int k = 1; k < 8; ++k) pre[k] = pre[k - 1] + r[k];
-    const double incl2 = warp_incl_scan_d((double)pre[7], lane);
-    const double base = pexcl + incl2 - (double)pre[7];
+    const DF incl2 = warp_incl_scan_df({pre[7], 0.f}, lane);
+    const DF base = df_add(pexcl, df_add_f(incl2, -pre[7]));  // prefix before this lane's 8
     const int v0 = jstar * kSubChunk + lane * 8;
     int c2 = INT_MAX, back = -1;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      if (c2 == INT_MAX && r[k] > 0.f && base + (double)pre[k] > T) c2 = v0 + k;
+      if (c2 == INT_MAX && r[k] > 0.f && df_gt(df_add_f(base, pre[k]), T)) c2 = v0 + k;
       if (r[k] > 0.f) back = v0 + k;
     }
     c2 = warp_min_i(c2);

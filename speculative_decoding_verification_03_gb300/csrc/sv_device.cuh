@@ -51,11 +51,11 @@ __device__ __forceinline__ U32x4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
 }
 
 // Uniform for (seed, sequence b, position pos): word `draw` of the block with
-// counter (b, pos, 0, 0); the top 24 bits scaled by 2^-24 (exact in fp32 and
-// fp64).  Draw 0 = acceptance, draw 1 = residual/bonus sampling.
-__device__ __forceinline__ double uniform24(uint64_t seed, uint32_t b, uint32_t pos, int draw) {
+// counter (b, pos, 0, 0); the top 24 bits scaled by 2^-24 (exact in fp32).
+// Draw 0 = acceptance, draw 1 = residual/bonus sampling.
+__device__ __forceinline__ float uniform24f(uint64_t seed, uint32_t b, uint32_t pos, int draw) {
   const U32x4 r = philox4x32_10(b, pos, 0u, 0u, (uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32));
-  return (double)(r.w[draw & 3] >> 8) * (1.0 / 16777216.0);
+  return (float)(r.w[draw & 3] >> 8) * (1.0f / 16777216.0f);
 }
 
 // ---------------------------------------------------------------------------

@@ -14,7 +14,7 @@ constexpr int kStageBytes = 49152;                 // one TMA bulk copy
 constexpr int kStages = 4;                         // ring depth (192 KB in flight per SM)
 constexpr int kConsumerWarps = 12;
 constexpr int kConsumers = kConsumerWarps * 32;    // 384 math threads
-constexpr int kEpiWarps = 2;                       // epilogue warps (items alternate between them)
+constexpr int kEpiWarps = 3;                       // epilogue warps (take items from a shared counter)
 constexpr int kPartSlots = 8;                      // finished items the math warps may run ahead
 constexpr int kRowThreads = kConsumers + 32 + 32 * kEpiWarps;  // + producer warp + epilogue warps
 constexpr int kVecPerStage = kStageBytes / 16;     // 3072 16-byte vectors
@@ -109,6 +109,15 @@ struct RowPassParams {
   uint32_t *dq_tail;   // slots reserved by publishers
   uint32_t *dq_head;   // slots claimed by producers
   SampleParams smp;
+  // fused AV refit (sv_verify_fit): every scan adds its labels' terms to
+  // fitacc as 2^-32 fixed point; the last scan updates the round
+  int fit;
+  int round_len;
+  float damping_c;
+  float *theta_rw;
+  unsigned char *av_state;
+  unsigned long long *fitacc;  // [SV_MAX_K][kFitQ]
+  uint32_t *scans_done;
 };
 
 
@@ -117,7 +126,7 @@ constexpr int kMaxSampleParts = 16;
 
 struct WsLayout {
   size_t counters_off, counters_bytes;  // zeroed by every call
-  size_t ticket_off, row_cnt_off, seq_cnt_off, smp_cnt_off, dq_off;
+  size_t ticket_off, fitacc_off, row_cnt_off, seq_cnt_off, smp_cnt_off, dq_off;
   size_t stats_off, chunk_off, task_off, subsum_off;
   size_t total;
 };
@@ -130,8 +139,10 @@ inline WsLayout ws_layout(int B, int K, int V) {
   const size_t nsub = ((size_t)V + kSubChunk - 1) / kSubChunk;
   size_t off = 256;  // status word and spare header
   L.counters_off = off;
-  L.ticket_off = off;  // ticket, dq_tail, dq_head
+  L.ticket_off = off;  // ticket, dq_tail, dq_head, scans_done
   off += 16;
+  L.fitacc_off = off;  // [SV_MAX_K][6] 64-bit fixed point
+  off += (size_t)SV_MAX_K * 6 * 8;
   L.row_cnt_off = off;
   off += nrow * 4;
   L.seq_cnt_off = off;
