@@ -323,13 +323,13 @@ struct Elems<SV_FP32> {
 // in shared memory (the stage is this warp's until released, and only this
 // lane reads that vector), then the lane sums are rescaled.
 template <int kDtype>
-__device__ __forceinline__ void stage_rise(WarpState &s, uint4 *ring, const float (&vm)[kVecPerThread], int tid,
-                                           int lane, int e0, float c, float wm) {
+__device__ __forceinline__ void stage_rise(WarpState &s, uint4 *ring, int nvec, int tid, int lane, int e0, float c,
+                                           float wm) {
   using E = Elems<kDtype>;
   int jv = -1;
 #pragma unroll
   for (int j = kVecPerThread - 1; j >= 0; --j)
-    if (vm[j] == wm) jv = j;
+    if (tid + j * kConsumers < nvec && E::vmax1(ring[tid + j * kConsumers]) == wm) jv = j;
   int cand = INT_MAX;
   if (jv >= 0) {
     const int vi = tid + jv * kConsumers;
@@ -370,21 +370,22 @@ __device__ __forceinline__ void consume_stage(WarpState &s, uint4 *ring, int nve
                                               float c) {
   using E = Elems<kDtype>;
   const uint4 *base = ring + tid;
-  float vm[kVecPerThread];
   const bool full = nvec == kVecPerStage;
+  float lm;
   if (full) {
+    uint4 w[kVecPerThread];
 #pragma unroll
-    for (int j = 0; j < kVecPerThread; ++j) vm[j] = E::vmax1(base[j * kConsumers]);
+    for (int j = 0; j < kVecPerThread; ++j) w[j] = base[j * kConsumers];
+    lm = E::vmax(w);
   } else {
+    lm = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kVecPerThread; ++j)
-      vm[j] = (tid + j * kConsumers < nvec) ? E::vmax1(base[j * kConsumers]) : -INFINITY;
+      if (tid + j * kConsumers < nvec) lm = fmaxf(lm, E::vmax1(base[j * kConsumers]));
   }
-  float lm = vm[0];
-#pragma unroll
-  for (int j = 1; j < kVecPerThread; ++j) lm = fmaxf(lm, vm[j]);
   const float wm = warp_max(lm);
-  if (wm > s.M) stage_rise<kDtype>(s, ring, vm, tid, lane, e0, c, wm);  // warp-uniform
+  // the per-vector maxima are recomputed only when the warp max rises (rare)
+  if (wm > s.M) stage_rise<kDtype>(s, ring, nvec, tid, lane, e0, c, wm);  // warp-uniform
   const float2 cc = make_float2(c, c), nb = make_float2(s.nbh, s.nbh);
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   if (full) {
