@@ -238,3 +238,13 @@ class AVFit:
             self.acc = None
             self.steps = 0
         return status
+
+
+# --------------------------------------------------------------------------
+# The steps around verification, in plain numpy (budget.py, post_verify.py,
+# tts.py, tree.py)
+# --------------------------------------------------------------------------
+from .budget import av_budget, survival  # noqa: E402
+from .post_verify import post_verify  # noqa: E402
+from .tree import tree_uniform, verify_tree  # noqa: E402
+from .tts import tts_signal  # noqa: E402
