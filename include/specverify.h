@@ -233,6 +233,81 @@ sv_status_t sv_verify_fit(int B, int K, int V, sv_dtype_t dtype,
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sv_av_budget -- AV's global draft budget, the step before verification.
+ *
+ * Defined by "Adaptive Verification without a confidence head", section
+ * "Other features considered": drafts are ranked by survival (the running
+ * product of the confidences along each request), the estimated number of
+ * accepted tokens of a budget of n drafts is n_req plus the n largest
+ * survivals, and the budget is the n maximising that estimate divided by the
+ * cost of drafting and verifying n tokens; the n best drafts are kept.
+ *
+ *   conf          device float [B][K]: per-position confidences (sv_av_score
+ *                 or sv_verify); survival s[b][i] = fl32 running product in
+ *                 position order; NaN survivals are not candidates, values
+ *                 at or below 0 count as 0
+ *   draft_len     device int32 [B] or NULL: only positions i < draft_len[b]
+ *                 are candidates (clamped to [0, K])
+ *   n_req         number of sampling requests (est[0])
+ *   draft_cost, verify_cost  device float [N + 1] at least (N = number of
+ *                 candidates <= B*K): cost of n drafted / verified tokens
+ *   out_budget    device int32 [1]: the first n maximising est[n] / cost[n]
+ *                 over the n with cost[n] > 0 and a finite ratio (0 if none);
+ *                 est[n] sums the ranked survivals in fp64 (ranking: survival
+ *                 descending, then b*K + i ascending)
+ *   out_kept_len  device int32 [B]: drafts of request b among the n best; they
+ *                 are its first out_kept_len[b] positions
+ * B*K <= SV_BUDGET_MAX.  One CTA; returns after enqueueing.
+ * ---------------------------------------------------------------------- */
+#define SV_BUDGET_MAX 16384
+sv_status_t sv_av_budget(int B, int K, const float *conf, const int32_t *draft_len, int n_req,
+                         const float *draft_cost, const float *verify_cost,
+                         int32_t *out_budget, int32_t *out_kept_len, void *stream);
+
+/* ------------------------------------------------------------------------
+ * sv_post_verify -- the step after verification, on the device, so that the
+ * host never waits for the accepted lengths.
+ *
+ * Defined by "Accelerating Sonar through Speculation", section "MTP schedule
+ * for one token" (a kernel shifts the target's input tokens and plugs the
+ * target's next token into its position; the draft then re-runs on the same
+ * batch layout) and the "Speculative Decoding: Draft, EAGLE, MTP" cheatsheet,
+ * "algorithm loop in code" (the key-value cache grows by one entry per
+ * accepted draft; at the first rejection it is cut back to the prefix length
+ * plus the number of emitted tokens).  For sequence b with a = accept_len[b]
+ * and k = draft_len[b] (K when NULL):
+ *   next_in[b][j] = out_tokens[b][j]        for j <= a
+ *                 = in_tokens[b][j + 1]     for a < j < k  (drafts the next
+ *                                           step recomputes and discards)
+ *                 = -1                      otherwise
+ *   history[b][seq_len[b] + j] = out_tokens[b][j] for j <= a (positions at or
+ *                 beyond history_cap are skipped: SV_PV_OVERFLOW)
+ *   seq_len[b] += a + 1
+ *   kv_len[b]  += a + 1 when a < k (rejection), k when all were accepted
+ *                 (the bonus token has no cache entry yet)
+ *
+ *   in_tokens    device int32 [B][K+1]: the verify input, [t_last, d_0 ..
+ *                d_{K-1}]; required when next_in is given
+ *   out_tokens   device int32 [B][K+1]: sv_verify's emitted tokens
+ *   accept_len   device int32 [B]: sv_verify's accept lengths
+ *   draft_len    device int32 [B] or NULL: as given to sv_verify
+ *   seq_len, kv_len  device int32 [B], updated in place
+ *   history      device int32 [B][history_cap] or NULL, updated in place
+ *   next_in      device int32 [B][K+1] or NULL (must not alias in_tokens)
+ *   flags        device uint32 [B] or NULL: SV_PV_* bits of each sequence;
+ *                a sequence with SV_PV_BAD_INPUT (accept_len outside
+ *                [0, k], or out_tokens[b][a] < 0) is left unchanged and its
+ *                next_in row is all -1.
+ * One warp per sequence; returns after enqueueing.
+ * ---------------------------------------------------------------------- */
+#define SV_PV_OVERFLOW  (1u << 0)
+#define SV_PV_BAD_INPUT (1u << 1)
+sv_status_t sv_post_verify(int B, int K, const int32_t *in_tokens, const int32_t *out_tokens,
+                           const int32_t *accept_len, const int32_t *draft_len,
+                           int32_t *seq_len, int32_t *kv_len, int32_t *history, int history_cap,
+                           int32_t *next_in, uint32_t *flags, void *stream);
+
+/* ------------------------------------------------------------------------
  * sv_philox -- the uniform stream itself, for checking: out[b][pos][w] =
  * word w of Philox4x32-10 with key (seed & 0xffffffff, seed >> 32) and
  * counter (b, pos, 0, 0) (Salmon, Moraes, Dror, Shaw, "Parallel Random

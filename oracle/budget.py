@@ -20,7 +20,9 @@ Readings where the page leaves a step open (also listed in the design doc):
     of candidates), summed in fp64 in ranking order; cost[n] = draft_cost[n] +
     verify_cost[n] from a cost table of at least N + 1 entries (synthetic
     here: the page's table is measured on its serving system);
-  - budget = the first n attaining the maximum of est[n] / cost[n];
+  - a survival that is NaN is not a candidate; one at or below 0 counts as 0;
+  - budget = the first n attaining the maximum of est[n] / cost[n] over the n
+    with cost[n] > 0 and a finite ratio (0 when there is none);
   - kept_len[b] = the number of request b's drafts among the n best.
 """
 from __future__ import annotations
@@ -47,7 +49,8 @@ def av_budget(conf, n_req: int, draft_cost, verify_cost, draft_len=None):
     B, K = c.shape
     s = survival(c)
     kl = np.full(B, K, np.int64) if draft_len is None else np.clip(np.asarray(draft_len), 0, K)
-    cand = [(float(s[b, i]), b * K + i) for b in range(B) for i in range(int(kl[b]))]
+    cand = [(max(float(s[b, i]), 0.0), b * K + i) for b in range(B) for i in range(int(kl[b]))
+            if not np.isnan(s[b, i])]
     # survival descending, flat index ascending
     cand.sort(key=lambda t: (-t[0], t[1]))
     N = len(cand)
@@ -61,11 +64,12 @@ def av_budget(conf, n_req: int, draft_cost, verify_cost, draft_len=None):
     vc = np.asarray(verify_cost, dtype=np.float32).astype(np.float64)
     assert dc.size >= N + 1 and vc.size >= N + 1
     cost = dc[:N + 1] + vc[:N + 1]
-    ratio = est / cost
-    budget = 0
-    for n in range(1, N + 1):
-        if ratio[n] > ratio[budget]:
-            budget = n
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = est / cost
+    budget, best = 0, None
+    for n in range(N + 1):
+        if cost[n] > 0 and np.isfinite(ratio[n]) and (best is None or ratio[n] > best):
+            budget, best = n, ratio[n]
     kept = np.zeros(B, np.int32)
     for _, idx in cand[:budget]:
         kept[idx // K] += 1

@@ -18,7 +18,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = ["api.cu", "rowpass.cu", "sample.cu", "avfit.cu"]
+_SOURCES = ["api.cu", "rowpass.cu", "sample.cu", "avfit.cu", "postverify.cu", "budget.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC"]
 
@@ -96,6 +96,10 @@ def lib():
             L.sv_status.restype = I
             L.sv_set_launch_events.argtypes = [P, P]
             L.sv_set_launch_events.restype = I
+            L.sv_post_verify.argtypes = [I, I, P, P, P, P, P, P, P, I, P, P, P]
+            L.sv_post_verify.restype = I
+            L.sv_av_budget.argtypes = [I, I, P, P, I, P, P, P, P, P]
+            L.sv_av_budget.restype = I
             L.sv_strerror.argtypes = [I]
             L.sv_strerror.restype = ctypes.c_char_p
             _lib = L
@@ -275,6 +279,47 @@ class HostSession:
                damping_c=self.damping_c)
         tokens_out.copy_(self.out["tokens"], non_blocking=True)
         accept_out.copy_(self.out["accept_len"], non_blocking=True)
+
+
+def post_verify(in_tokens, out_tokens, accept_len, seq_len, kv_len, history=None, draft_len=None,
+                next_in=None, flags=None, stream=None):
+    """sv_post_verify: updates seq_len, kv_len and history in place, fills
+    next_in and flags (allocated when not given); returns (next_in, flags)."""
+    B, K1 = out_tokens.shape
+    dev = out_tokens.device
+    for t, n in ((in_tokens, "in_tokens"), (out_tokens, "out_tokens"), (accept_len, "accept_len"),
+                 (seq_len, "seq_len"), (kv_len, "kv_len"), (history, "history"), (draft_len, "draft_len")):
+        _dev(t, n, torch.int32)
+    if next_in is None:
+        next_in = torch.empty((B, K1), dtype=torch.int32, device=dev)
+    if flags is None:
+        flags = torch.empty((B,), dtype=torch.int32, device=dev)
+    cap = 0 if history is None else history.shape[1]
+    rc = lib().sv_post_verify(B, K1 - 1, _ptr(in_tokens), _ptr(out_tokens), _ptr(accept_len), _ptr(draft_len),
+                              _ptr(seq_len), _ptr(kv_len), _ptr(history), cap, _ptr(next_in), _ptr(flags),
+                              _stream(stream))
+    _check(rc, "sv_post_verify")
+    return next_in, flags
+
+
+def av_budget(conf, n_req: int, draft_cost, verify_cost, draft_len=None, out_budget=None, out_kept_len=None,
+              stream=None):
+    """sv_av_budget: returns (budget [1] int32, kept_len [B] int32) device tensors."""
+    B, K = conf.shape
+    _dev(conf, "conf", torch.float32)
+    _dev(draft_cost, "draft_cost", torch.float32)
+    _dev(verify_cost, "verify_cost", torch.float32)
+    _dev(draft_len, "draft_len", torch.int32)
+    if draft_cost.numel() < B * K + 1 or verify_cost.numel() < B * K + 1:
+        raise ValueError("cost tables need B*K + 1 entries")
+    if out_budget is None:
+        out_budget = torch.empty((1,), dtype=torch.int32, device=conf.device)
+    if out_kept_len is None:
+        out_kept_len = torch.empty((B,), dtype=torch.int32, device=conf.device)
+    rc = lib().sv_av_budget(B, K, _ptr(conf), _ptr(draft_len), int(n_req), _ptr(draft_cost), _ptr(verify_cost),
+                            _ptr(out_budget), _ptr(out_kept_len), _stream(stream))
+    _check(rc, "sv_av_budget")
+    return out_budget, out_kept_len
 
 
 def status(holder: torch.Tensor, stream=None):

@@ -18,6 +18,12 @@ cudaError_t launch_philox(uint64_t seed, int nb, int npos, uint32_t *out, cudaSt
 using namespace sv;
 
 namespace {
+sv_status_t device_info(int *sms);
+}
+
+sv_status_t sv::host_device_info(int *sms) { return device_info(sms); }
+
+namespace {
 
 constexpr int kMaxB = 1 << 20;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per wait

@@ -1,0 +1,186 @@
+// AV global draft budget ("Adaptive Verification without a confidence
+// head", section "Other features considered"): rank every draft by its
+// survival probability (running product of the confidences along its
+// request), estimate the accepted tokens of a budget of n drafts as the
+// number of requests plus the n largest survivals, and keep the n that
+// maximises estimate / (draft cost + verify cost).  One CTA: survivals and
+// 64-bit sort keys in shared memory, a bitonic sort, an fp64 block scan of
+// the ranked survivals, an argmax, and per-request kept counts.
+#include <cfloat>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr int kBudgetThreads = 1024;
+
+struct BudgetParams {
+  int B, K, n_req, npad;
+  const float *conf;
+  const int32_t *draft_len;
+  const float *draft_cost, *verify_cost;
+  int32_t *out_budget, *out_kept;
+};
+
+// Key of a candidate: survival descending (its fp32 bits, non-negative, so
+// the bit pattern orders like the value), then flat index ascending.
+// Non-candidates get the largest key.
+__device__ __forceinline__ uint64_t budget_key(float s, int idx) {
+  const uint32_t bits = s > 0.f ? __float_as_uint(s) : 0u;
+  return ((uint64_t)(0xffffffffu - bits) << 32) | (uint32_t)idx;
+}
+__device__ __forceinline__ float key_survival(uint64_t key) {
+  return __uint_as_float(0xffffffffu - (uint32_t)(key >> 32));
+}
+
+__device__ __forceinline__ double warp_incl_scan_f64(double v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const BudgetParams P) {
+  extern __shared__ uint64_t keys[];
+  __shared__ double s_wsum[kBudgetThreads / 32];
+  __shared__ double s_bratio[kBudgetThreads / 32];
+  __shared__ int s_bn[kBudgetThreads / 32];
+  __shared__ int s_ncand;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = P.B, K = P.K, NK = B * K, npad = P.npad;
+
+  if (tid == 0) s_ncand = 0;
+  for (int b = tid; b < B; b += kBudgetThreads) P.out_kept[b] = 0;
+  // 1. survivals (fp32 running product in position order) and keys
+  for (int b = tid; b < B; b += kBudgetThreads) {
+    int k = P.draft_len ? __ldg(P.draft_len + b) : K;
+    k = k < 0 ? 0 : (k > K ? K : k);
+    float run = 1.f;
+    for (int i = 0; i < K; ++i) {
+      run = __fmul_rn(run, __ldg(P.conf + (size_t)b * K + i));
+      const bool cand = i < k && !isnan(run);
+      keys[b * K + i] = cand ? budget_key(run, b * K + i) : ~0ull;
+    }
+  }
+  for (int j = NK + tid; j < npad; j += kBudgetThreads) keys[j] = ~0ull;
+  __syncthreads();
+
+  // 2. bitonic sort, ascending keys
+  for (int size = 2; size <= npad; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = tid; t < (npad >> 1); t += kBudgetThreads) {
+        const int lo = 2 * stride * (t / stride) + (t % stride), hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const uint64_t x = keys[lo], y = keys[hi];
+        if ((x > y) == up) {
+          keys[lo] = y;
+          keys[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // 3. number of candidates: the first non-candidate key
+  for (int j = tid; j < npad; j += kBudgetThreads)
+    if (keys[j] != ~0ull && (j + 1 == npad || keys[j + 1] == ~0ull)) s_ncand = j + 1;
+  __syncthreads();
+  const int N = s_ncand;
+
+  // 4. est[n] = n_req + sum of the n first ranked survivals (fp64): each
+  //    thread a contiguous segment, block scan of the segment sums
+  const int per = (N + kBudgetThreads - 1) / kBudgetThreads;
+  const int j0 = min(N, tid * per), j1 = min(N, j0 + per);
+  double seg = 0.0;
+  for (int j = j0; j < j1; ++j) seg += (double)key_survival(keys[j]);
+  double incl = warp_incl_scan_f64(seg, lane);
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const double w = warp_incl_scan_f64(s_wsum[lane], lane);
+    s_wsum[lane] = w;
+  }
+  __syncthreads();
+  double run = (double)P.n_req + (warp > 0 ? s_wsum[warp - 1] : 0.0) + (incl - seg);
+  // 5. ratio est[n] / cost[n] and its first maximum over the eligible n
+  double best = -DBL_MAX;
+  int bn = INT_MAX;
+  auto consider = [&](int n, double est) {
+    const double cost = (double)__ldg(P.draft_cost + n) + (double)__ldg(P.verify_cost + n);
+    if (!(cost > 0.0)) return;
+    const double r = est / cost;
+    if (isfinite(r) && r > best) {
+      best = r;
+      bn = n;
+    }
+  };
+  if (tid == 0) consider(0, (double)P.n_req);
+  for (int j = j0; j < j1; ++j) {
+    run += (double)key_survival(keys[j]);
+    consider(j + 1, run);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int on = __shfl_xor_sync(0xffffffffu, bn, o);
+    if (ob > best || (ob == best && on < bn)) {
+      best = ob;
+      bn = on;
+    }
+  }
+  if (lane == 0) {
+    s_bratio[warp] = best;
+    s_bn[warp] = bn;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    best = s_bratio[lane];
+    bn = s_bn[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int on = __shfl_xor_sync(0xffffffffu, bn, o);
+      if (ob > best || (ob == best && on < bn)) {
+        best = ob;
+        bn = on;
+      }
+    }
+    if (lane == 0) s_bn[0] = bn == INT_MAX ? 0 : bn;
+  }
+  __syncthreads();
+  const int budget = s_bn[0];
+  if (tid == 0) P.out_budget[0] = budget;
+  // 6. kept drafts per request
+  for (int j = tid; j < budget; j += kBudgetThreads) atomicAdd(P.out_kept + (int)(uint32_t)keys[j] / K, 1);
+}
+
+}  // namespace
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" sv_status_t sv_av_budget(int B, int K, const float *conf, const int32_t *draft_len, int n_req,
+                                    const float *draft_cost, const float *verify_cost, int32_t *out_budget,
+                                    int32_t *out_kept_len, void *stream) {
+  if (B < 0 || K < 0 || K > SV_MAX_K || (long long)B * K > SV_BUDGET_MAX) return SV_ERR_INVALID;
+  if (!out_budget || !out_kept_len || !draft_cost || !verify_cost || (B * K > 0 && !conf)) return SV_ERR_INVALID;
+  const void *ptrs[] = {conf, draft_len, draft_cost, verify_cost, out_budget, out_kept_len};
+  for (const void *p : ptrs)
+    if (!host_aligned(p, 4)) return SV_ERR_INVALID;
+  int sms = 0;
+  const sv_status_t ds = host_device_info(&sms);
+  if (ds != SV_OK) return ds;
+  int npad = 2;
+  while (npad < B * K) npad <<= 1;
+  const size_t smem = (size_t)npad * sizeof(uint64_t);
+  const cudaError_t e = cudaFuncSetAttribute(av_budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(SV_BUDGET_MAX * sizeof(uint64_t)));
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  BudgetParams P{B, K, n_req, npad, conf, draft_len, draft_cost, verify_cost, out_budget, out_kept_len};
+  av_budget_kernel<<<1, kBudgetThreads, smem, static_cast<cudaStream_t>(stream)>>>(P);
+  return host_cuda_status(cudaGetLastError());
+}

@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_runtime.h>
+
 #include "specverify.h"
 
 namespace sv {
@@ -183,6 +185,12 @@ struct AvStateHeader {
 constexpr size_t kAvAccOff = 256;
 constexpr size_t kAvAccDoubles = 4 * SV_MAX_K + 2;
 constexpr size_t kAvPartOff = align_up(kAvAccOff + kAvAccDoubles * 8, 256);
+
+// ---- host helpers shared by the entry points (api.cu) ------------------------
+// SM count of the current device; SV_ERR_UNSUPPORTED unless it is sm_103.
+sv_status_t host_device_info(int *sms);
+inline sv_status_t host_cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
+inline bool host_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 struct FitParams {
   int B, K, round_len;

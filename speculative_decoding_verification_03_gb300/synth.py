@@ -215,8 +215,31 @@ def logits_np(t: torch.Tensor):
     return t.numpy()
 
 
+def budget_inputs(B: int, K: int, seed: int = 0):
+    """Inputs of the AV budget step: confidences conf[b][i] ~ Beta with mean
+    0.88 - 0.035 i (later positions less certain), and synthetic cost tables
+    of N + 1 = B K + 1 entries in milliseconds: a drafter whose cost grows
+    slowly with the drafted tokens, and a target forward pass whose cost grows
+    in steps of 64 tokens (B requests plus n drafts), with 1 % seeded jitter.
+    The pages' tables are measured on their serving system."""
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    mean = np.clip(0.88 - 0.035 * np.arange(K), 0.05, 0.95)
+    conc = 12.0
+    x = rng.gamma(mean * conc, size=(B, K))
+    y = rng.gamma((1 - mean) * conc, size=(B, K))
+    conf = torch.from_numpy(x / (x + y)).to(torch.float32)
+    n = torch.arange(B * K + 1, dtype=torch.float64)
+    jitter = 1.0 + 0.01 * (torch.from_numpy(rng.random(B * K + 1)) - 0.5)
+    draft_cost = ((0.9 + 0.0012 * n) * jitter).to(torch.float32)
+    verify_cost = ((11.0 + 0.0035 * 64 * torch.ceil((B + n) / 64)) * jitter).to(torch.float32)
+    return conf, draft_cost, verify_cost
+
+
 WORKLOADS = dict(tiny=tiny, c2=c2, c3=c3, c4=c4, c5=c5)
 
 __all__ = ["Workload", "WORKLOADS", "tiny", "c2", "c3", "c4", "c5", "alpha_exact", "two_token_example",
+           "budget_inputs",
            "logits_np", "PEAK_BOOST"]
 
