@@ -265,6 +265,86 @@ sv_status_t sv_av_budget(int B, int K, const float *conf, const int32_t *draft_l
                          int32_t *out_budget, int32_t *out_kept_len, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sv_tts_signal -- the test-time-speculation distillation signal on the
+ * verified rows.
+ *
+ * Defined by "Technical summary: Test-Time Speculation (TTS)", section
+ * "Algorithm", step 3 "Distillation loss": after verification the drafter
+ * takes a gradient step on KL~(p || q) + lambda KL~(q_t || q) over the
+ * canvas with position weights w_k; at q = q_t the second term and its
+ * gradient vanish.  For request b and canvas position k < K, with
+ * p = softmax(target row k / tau_b), q = softmax(draft row k / tau_b)
+ * (tau_b <= 0 counts as 1):
+ *   out_kl[b][k]      = w_k * sum_v p_v (ln p_v - ln q_v)
+ *   out_grad[b][k][v] = w_k * (q_v - p_v) / tau_b     (bf16, round to nearest
+ *                       even: the gradient of out_kl with respect to the
+ *                       draft logits)
+ *
+ *   target_logits  device [B][K+1][V] (the sv_verify layout; rows 0..K-1 read)
+ *   draft_logits   device [B][K][V]
+ *   temperature    device float [B]
+ *   weights        device float [K]
+ *   out_kl         device float [B][K]
+ *   out_grad       device bf16 bits [B][K][V] or NULL (KL only)
+ * Reads every row pair twice (the second time mostly from L2) and writes
+ * the gradient once.  Returns after enqueueing.
+ * ---------------------------------------------------------------------- */
+sv_status_t sv_tts_signal(int B, int K, int V, sv_dtype_t dtype, const void *target_logits,
+                          const void *draft_logits, const float *temperature, const float *weights,
+                          float *out_kl, uint16_t *out_grad, void *stream);
+
+/* ------------------------------------------------------------------------
+ * sv_verify_tree -- verification of a token tree (several draft branches per
+ * request) in one call: the acceptance walk only (the target's tree
+ * attention mask is the caller's).
+ *
+ * Defined by "Accelerating Sonar through Speculation", section "EAGLE" (the
+ * drafter explores a tree of candidates; the target scores it in one pass;
+ * the best-fitting branch is kept and one target token appended), with the
+ * rule of the "Speculative Decoding: Draft, EAGLE, MTP" cheatsheet, "one
+ * speculative step", applied at every node: at the current node c the
+ * children are tried in ascending node order; child j with token x is
+ * accepted iff U < p_j(x) / q(x), where p_0 = softmax(target row c / tau),
+ * q = softmax(draft row c / tau), and after each rejected child
+ * p_{j+1} = max(p_j - q, 0) normalised.  An accepted child becomes the
+ * current node; when no child is accepted, or c is a leaf, one token is
+ * drawn from the last p_j (smallest v whose cumulative mass exceeds U' times
+ * the total) and the walk ends.  Children are assumed drawn independently
+ * from the draft distribution at their parent (with replacement), the
+ * setting in which this rule is lossless.  Greedy rows (tau <= 0): the first
+ * child equal to the target argmax (lowest index on ties) is accepted; else,
+ * and at a leaf, the argmax is emitted.
+ *
+ *   N             nodes per request (1..SV_TREE_MAX_NODES); node 0 is the last
+ *                 committed token, node n >= 1 carries tokens[b][n] and has
+ *                 parents[b][n] in [0, n)
+ *   target_logits device [B][N][V]: row n = the target's next-token logits
+ *                 after node n
+ *   draft_logits  device [B][N][V]: row n = the draft logits after node n,
+ *                 from which node n's children were drawn
+ *   n_nodes       device int32 [B] or NULL (= N): nodes in use per request
+ *   temperature   device float [B]
+ *   seed          Philox4x32-10 key: the test of child j at depth t uses word 0
+ *                 of block (b, t, j, 0); the final draw at depth t word 1 of
+ *                 block (b, t, 0, 0) -- a chain tree reproduces sv_verify
+ *   out_tokens    device int32 [B][N]: emitted tokens, then -1
+ *   out_accept_len device int32 [B]: accepted draft tokens (the path depth)
+ *   out_path      device int32 [B][max(N-1,1)] or NULL: accepted node indices
+ *   out_flags     device uint32 [B] or NULL: SV_TREE_* bits; a request with
+ *                 SV_TREE_BAD (a parent outside [0, n), n_nodes outside
+ *                 [1, N]) emits nothing (all -1, accept_len 0)
+ * One CTA per request; every row read stays in L2 for its later passes.
+ * ---------------------------------------------------------------------- */
+#define SV_TREE_MAX_NODES 64
+#define SV_TREE_ZERO_RESIDUAL (1u << 0) /* a residual had no mass (rounding); the previous p kept */
+#define SV_TREE_BAD           (1u << 1)
+sv_status_t sv_verify_tree(int B, int N, int V, sv_dtype_t dtype, const void *target_logits,
+                           const void *draft_logits, const int32_t *tokens, const int32_t *parents,
+                           const int32_t *n_nodes, const float *temperature, uint64_t seed,
+                           int32_t *out_tokens, int32_t *out_accept_len, int32_t *out_path,
+                           uint32_t *out_flags, void *stream);
+
+/* ------------------------------------------------------------------------
  * sv_post_verify -- the step after verification, on the device, so that the
  * host never waits for the accepted lengths.
  *

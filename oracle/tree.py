@@ -57,20 +57,26 @@ def _softmax(z):
 
 
 def _draw(p, u):
-    """Smallest v with C(v) > u * R, C the ascending cumulative sum of p."""
+    """Smallest v with C(v) > u * R, C the ascending cumulative sum of p;
+    also the distance of u * R to the nearer edge of v's step, over R."""
     c = np.cumsum(p)
     R = c[-1]
     idx = np.nonzero(c > u * R)[0]
     if idx.size:
-        return int(idx[0])
+        v = int(idx[0])
+        lo = c[v - 1] if v > 0 else 0.0
+        return v, min(u * R - lo, c[v] - u * R) / R
     nz = np.nonzero(p > 0)[0]
-    return int(nz[-1]) if nz.size else int(np.argmax(p))
+    return (int(nz[-1]) if nz.size else int(np.argmax(p))), 0.0
 
 
-def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=None):
+def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=None, seq_ids=None):
     """target, draft [B][N][V] floats; tokens, parents [B][N] int; temperature [B].
     Returns dict(tokens [B][N] (emitted, -1 after), accept_len [B], path [B][N-1]
-    (accepted node indices, -1 after), flags [B])."""
+    (accepted node indices, -1 after), flags [B], margin [B]: the smallest
+    distance of a decision to its boundary -- |u - p(x)/q(x)| over the child
+    tests and the final draw's distance to its step edge (over R)).
+    seq_ids [B] or None: the request indices that key the uniforms."""
     t = np.asarray(target, dtype=np.float64)
     d = np.asarray(draft, dtype=np.float64)
     tok = np.asarray(tokens, dtype=np.int64)
@@ -82,7 +88,10 @@ def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=
     path = np.full((B, max(N - 1, 1)), -1, np.int32)
     acc = np.zeros(B, np.int32)
     flags = np.zeros(B, np.int32)
+    margin = np.full(B, np.inf)
+    sid = np.arange(B) if seq_ids is None else np.asarray(seq_ids, dtype=np.int64)
     for b in range(B):
+        key = int(sid[b])
         n_b = int(nn[b])
         if n_b < 1 or n_b > N or any(not (0 <= par[b, n] < n) for n in range(1, n_b)):
             flags[b] |= FLAG_BAD_TREE
@@ -104,10 +113,11 @@ def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=
                 nxt = None
                 for j, c in enumerate(kids):
                     x = int(tok[b, c])
-                    u = tree_uniform(seed, b, depth, j, 0)
+                    u = tree_uniform(seed, key, depth, j, 0)
                     ratio = 0.0
                     if 0 <= x < V:
                         ratio = np.inf if q[x] == 0 else p[x] / q[x]
+                    margin[b] = min(margin[b], abs(u - ratio))
                     if u < ratio:
                         nxt = c
                         break
@@ -117,11 +127,12 @@ def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=
                     else:
                         flags[b] |= FLAG_ZERO_RESIDUAL
                 if nxt is None:
-                    out[b, depth] = _draw(p, tree_uniform(seed, b, depth, 0, 1))
+                    out[b, depth], m = _draw(p, tree_uniform(seed, key, depth, 0, 1))
+                    margin[b] = min(margin[b], m)
                     break
             out[b, depth] = tok[b, nxt]
             path[b, depth] = nxt
             cur = nxt
             depth += 1
         acc[b] = depth
-    return dict(tokens=out, accept_len=acc, path=path, flags=flags)
+    return dict(tokens=out, accept_len=acc, path=path, flags=flags, margin=margin)

@@ -18,7 +18,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = ["api.cu", "rowpass.cu", "sample.cu", "avfit.cu", "postverify.cu", "budget.cu"]
+_SOURCES = ["api.cu", "rowpass.cu", "sample.cu", "avfit.cu", "postverify.cu", "budget.cu", "tts.cu", "tree.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC"]
 
@@ -100,6 +100,10 @@ def lib():
             L.sv_post_verify.restype = I
             L.sv_av_budget.argtypes = [I, I, P, P, I, P, P, P, P, P]
             L.sv_av_budget.restype = I
+            L.sv_tts_signal.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
+            L.sv_tts_signal.restype = I
+            L.sv_verify_tree.argtypes = [I, I, I, I, P, P, P, P, P, P, U64, P, P, P, P, P]
+            L.sv_verify_tree.restype = I
             L.sv_strerror.argtypes = [I]
             L.sv_strerror.restype = ctypes.c_char_p
             _lib = L
@@ -320,6 +324,51 @@ def av_budget(conf, n_req: int, draft_cost, verify_cost, draft_len=None, out_bud
                             _ptr(out_budget), _ptr(out_kept_len), _stream(stream))
     _check(rc, "sv_av_budget")
     return out_budget, out_kept_len
+
+
+def tts_signal(target, draft, temperature, weights, want_grad: bool = True, out_kl=None, out_grad=None,
+               stream=None):
+    """sv_tts_signal: returns (kl [B][K] float32, grad [B][K][V] bfloat16 or None)."""
+    B, K, V = draft.shape
+    code = _dtype_code(target)
+    if _dtype_code(draft) != code or target.shape != (B, K + 1, V):
+        raise ValueError("target must be [B][K+1][V] and draft [B][K][V] of one dtype")
+    _dev(target, "target")
+    _dev(draft, "draft")
+    _dev(temperature, "temperature", torch.float32)
+    _dev(weights, "weights", torch.float32)
+    if out_kl is None:
+        out_kl = torch.empty((B, K), dtype=torch.float32, device=draft.device)
+    if want_grad and out_grad is None:
+        out_grad = torch.empty((B, K, V), dtype=torch.bfloat16, device=draft.device)
+    rc = lib().sv_tts_signal(B, K, V, code, _ptr(target), _ptr(draft), _ptr(temperature), _ptr(weights),
+                             _ptr(out_kl), _ptr(out_grad) if want_grad else None, _stream(stream))
+    _check(rc, "sv_tts_signal")
+    return out_kl, (out_grad if want_grad else None)
+
+
+def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=None, stream=None):
+    """sv_verify_tree: returns dict(tokens [B][N], accept_len [B], path [B][N-1], flags [B])."""
+    B, N, V = target.shape
+    code = _dtype_code(target)
+    if _dtype_code(draft) != code or draft.shape != target.shape:
+        raise ValueError("target and draft must both be [B][N][V] of one dtype")
+    for t, n in ((target, "target"), (draft, "draft")):
+        _dev(t, n)
+    for t, n in ((tokens, "tokens"), (parents, "parents"), (n_nodes, "n_nodes")):
+        _dev(t, n, torch.int32)
+    _dev(temperature, "temperature", torch.float32)
+    dev = target.device
+    out = dict(tokens=torch.empty((B, N), dtype=torch.int32, device=dev),
+               accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
+               path=torch.empty((B, max(N - 1, 1)), dtype=torch.int32, device=dev),
+               flags=torch.empty((B,), dtype=torch.int32, device=dev))
+    rc = lib().sv_verify_tree(B, N, V, code, _ptr(target), _ptr(draft), _ptr(tokens), _ptr(parents),
+                              _ptr(n_nodes), _ptr(temperature), ctypes.c_uint64(int(seed) & (2**64 - 1)),
+                              _ptr(out["tokens"]), _ptr(out["accept_len"]), _ptr(out["path"]), _ptr(out["flags"]),
+                              _stream(stream))
+    _check(rc, "sv_verify_tree")
+    return out
 
 
 def status(holder: torch.Tensor, stream=None):

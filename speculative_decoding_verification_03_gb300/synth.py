@@ -237,9 +237,64 @@ def budget_inputs(B: int, K: int, seed: int = 0):
     return conf, draft_cost, verify_cost
 
 
+@dataclass
+class TreeWorkload:
+    B: int
+    N: int
+    V: int
+    dtype: torch.dtype
+    target: torch.Tensor       # [B][N][V]: target logits after node n
+    draft: torch.Tensor        # [B][N][V]: draft logits after node n
+    tokens: torch.Tensor       # [B][N] int32 (node 0 unused)
+    parents: torch.Tensor      # [B][N] int32 (node 0: -1)
+    temperature: torch.Tensor  # [B] float32
+
+    def to(self, device) -> "TreeWorkload":
+        return TreeWorkload(self.B, self.N, self.V, self.dtype, self.target.to(device), self.draft.to(device),
+                            self.tokens.to(device), self.parents.to(device), self.temperature.to(device))
+
+
+def tree(seed: int = 0, B: int = 64, V: int = 32000, levels=(3, 6, 4, 2), dtype=torch.bfloat16,
+         boost: float = 8.0, greedy_frac: float = 0.1, device="cpu") -> TreeWorkload:
+    """Token trees in the shape of a static EAGLE-style tree: level sizes
+    `levels` below the root (node 0), every node's parent drawn uniformly
+    from the level above.  Per node, target logits z ~ N(0, 3^2) with one
+    token raised by `boost`, draft logits 0.8 z + N(0, 1.5^2); each child's
+    token is drawn independently from the softmax of its parent's draft row
+    at the request's temperature (argmax for greedy requests).  N = 1 +
+    sum(levels) nodes."""
+    g = _gen(seed, "cpu")
+    N = 1 + sum(levels)
+    parents = torch.full((B, N), -1, dtype=torch.int32)
+    n = 1
+    prev = [0]
+    for size in levels:
+        cur = list(range(n, n + size))
+        pick = torch.randint(0, len(prev), (B, size), generator=g)
+        parents[:, n:n + size] = torch.tensor(prev, dtype=torch.int32)[pick]
+        prev, n = cur, n + size
+    z = torch.randn((B, N, V), generator=g) * 3.0
+    hot = torch.randint(0, V, (B, N), generator=g)
+    z.scatter_add_(2, hot.unsqueeze(-1), torch.full((B, N, 1), boost))
+    d = 0.8 * z + torch.randn((B, N, V), generator=g) * 1.5
+    tau = torch.rand(B, generator=g) * 0.9 + 0.4
+    tau[torch.rand(B, generator=g) < greedy_frac] = 0.0
+    t_, d_ = z.to(dtype), d.to(dtype)
+    probs = torch.softmax(d_.float() / torch.where(tau > 0, tau, 1.0).view(B, 1, 1), -1)
+    tokens = torch.zeros((B, N), dtype=torch.int32)
+    for m in range(1, N):
+        par = parents[:, m].long()
+        rows = probs[torch.arange(B), par]
+        drawn = torch.multinomial(rows, 1, generator=g).view(B)
+        am = d_.float()[torch.arange(B), par].argmax(-1)
+        tokens[:, m] = torch.where(tau > 0, drawn, am).to(torch.int32)
+    w = TreeWorkload(B, N, V, dtype, t_.contiguous(), d_.contiguous(), tokens, parents, tau.to(torch.float32))
+    return w.to(device) if str(device) != "cpu" else w
+
+
 WORKLOADS = dict(tiny=tiny, c2=c2, c3=c3, c4=c4, c5=c5)
 
 __all__ = ["Workload", "WORKLOADS", "tiny", "c2", "c3", "c4", "c5", "alpha_exact", "two_token_example",
-           "budget_inputs",
+           "budget_inputs", "tree", "TreeWorkload",
            "logits_np", "PEAK_BOOST"]
 

@@ -113,3 +113,146 @@ def test_post_verify_after_verify_c2():
     assert np.array_equal(nxt.cpu().numpy(), r["next_in"]) and np.array_equal(hist.cpu().numpy(), r["history"])
     assert np.array_equal(sl.cpu().numpy(), r["seq_len"]) and np.array_equal(kv.cpu().numpy(), r["kv_len"])
     assert not fl.any()
+
+
+# ----------------------------------------------------------------------------- TTS
+def _tts_case(w, weights, pairs=None):
+    dev = torch.device("cuda")
+    g = w if w.target.is_cuda else w.to(dev)
+    wt = torch.tensor(weights, dtype=torch.float32, device=dev)
+    kl, grad = binding.tts_signal(g.target, g.draft, g.temperature, wt)
+    kl = kl.cpu().numpy()
+    t, d, tau = synth.logits_np(w.target), synth.logits_np(w.draft), w.temperature.cpu().numpy()
+    if w.target.dtype == torch.bfloat16:  # bf16 bit patterns -> values
+        t = (t.astype(np.uint32) << 16).view(np.float32)
+        d = (d.astype(np.uint32) << 16).view(np.float32)
+    if pairs is None:
+        pairs = [(b, k) for b in range(w.B) for k in range(w.K)]
+    for b, k in pairs:
+        r = oracle.tts_signal(t[b:b + 1, k:k + 1], d[b:b + 1, k:k + 1], tau[b:b + 1], [weights[k]])
+        ko = r["kl"][0, 0]
+        assert abs(kl[b, k] - ko) <= 1e-4 * abs(ko) + 1e-9, (b, k, kl[b, k], ko)
+        go = r["grad"][0, 0]
+        gg = grad[b, k].float().cpu().numpy()
+        tb = tau[b] if tau[b] > 0 else 1.0
+        p = np.exp(t[b, k] / tb - np.max(t[b, k] / tb))
+        p /= p.sum()
+        q = np.exp(d[b, k] / tb - np.max(d[b, k] / tb))
+        q /= q.sum()
+        # bf16 rounding, plus the fp32 normalisation of p and q (their sums
+        # over the row are kept to a few 1e-7): the error of q_v - p_v is
+        # bounded relative to the larger of the two
+        tol = 1.01 * 2.0**-8 * np.abs(go) + 2e-6 * weights[k] / tb * np.maximum(p, q) + 1e-38
+        bad = np.abs(gg - go) > tol
+        assert not bad.any(), (b, k, np.nonzero(bad)[0][:5], gg[bad][:5], go[bad][:5])
+    return kl
+
+
+def test_tts_tiny_and_unaligned():
+    w = synth.tiny(seed=3, B=6, K=4, V=64)
+    w.temperature = torch.tensor([1.0, 0.5, 0.0, 1.3, 1.0, 0.8])
+    _tts_case(w, [1.0, 0.9, 0.81, 0.729])
+    for V, dt in ((1001, torch.bfloat16), (37, torch.float32), (7, torch.bfloat16)):
+        g = torch.Generator().manual_seed(V)
+        z = torch.randn((5, 4, V), generator=g) * 2
+        dd = z[:, :3] + torch.randn((5, 3, V), generator=g) * 0.5
+        ww = synth.Workload("u", 5, 3, V, dt, z.to(dt).contiguous(), dd.to(dt).contiguous(),
+                            torch.zeros((5, 3), dtype=torch.int32), torch.ones(5))
+        _tts_case(ww, [1.0, 0.5, 0.25])
+
+
+def test_tts_identical_rows_give_zero():
+    w = synth.c2(seed=2)
+    w.draft = w.target[:, :w.K].contiguous()
+    dev = torch.device("cuda")
+    kl, grad = binding.tts_signal(w.target.to(dev), w.draft.to(dev), w.temperature.to(dev),
+                                  torch.ones(w.K, device=dev))
+    assert torch.all(kl.abs() < 1e-7) and torch.all(grad.float().abs() < 1e-7)
+
+
+def test_tts_c2_all_pairs():
+    w = synth.c2(seed=5)
+    _tts_case(w, [1.0, 0.8, 0.6, 0.4])
+
+
+def test_tts_c3_sampled_pairs():
+    w = synth.c3(seed=6, device="cuda")
+    rng = np.random.default_rng(0)
+    pairs = [(int(b), int(k)) for b, k in zip(rng.integers(0, w.B, 12), rng.integers(0, w.K, 12))]
+    kl = _tts_case(w, [1.0, 0.9, 0.8, 0.7, 0.6], pairs=pairs)
+    assert np.all(np.isfinite(kl)) and np.all(kl >= 0)
+
+
+# ----------------------------------------------------------------------------- tree
+TREE_TIE = 2e-5
+
+
+def _tree_values(t):
+    a = synth.logits_np(t)
+    return (a.astype(np.uint32) << 16).view(np.float32) if t.dtype == torch.bfloat16 else a
+
+
+def _tree_compare(w, seed, idx=None):
+    dev = torch.device("cuda")
+    g = w.to(dev)
+    out = binding.verify_tree(g.target, g.draft, g.tokens, g.parents, g.temperature, seed)
+    res = {k: v.cpu().numpy() for k, v in out.items()}
+    assert not (res["flags"] & 2).any()
+    sel = np.arange(w.B) if idx is None else np.asarray(idx)
+    T, D = _tree_values(w.target), _tree_values(w.draft)
+    r = oracle.verify_tree(T[sel], D[sel], w.tokens.numpy()[sel], w.parents.numpy()[sel],
+                           w.temperature.numpy()[sel], seed, seq_ids=sel)
+    ok = (res["accept_len"][sel] == r["accept_len"]) & np.all(res["tokens"][sel] == r["tokens"], axis=1) & \
+        np.all(res["path"][sel] == r["path"], axis=1)
+    tie = r["margin"] < TREE_TIE
+    bad = np.nonzero(~ok & ~tie)[0]
+    assert bad.size == 0, (sel[bad][:4], res["tokens"][sel][bad][:2], r["tokens"][bad][:2], r["margin"][bad][:4])
+    return res, r, int((~ok).sum()), int(tie.sum())
+
+
+@pytest.mark.parametrize("dtype,V", [(torch.float32, 300), (torch.bfloat16, 2000), (torch.bfloat16, 1001)])
+def test_tree_parity_small(dtype, V):
+    w = synth.tree(seed=V, B=48, V=V, dtype=dtype)
+    res, r, nbad, nties = _tree_compare(w, 17)
+    print("tree", V, "mismatch", nbad, "ties", nties, "mean accept", res["accept_len"].mean())
+    assert res["accept_len"].max() >= 2
+
+
+def test_tree_parity_vocab_32000_sampled():
+    w = synth.tree(seed=5, B=96, V=32000)
+    _tree_compare(w, 3, idx=np.arange(0, 96, 6))
+
+
+def test_tree_chain_equals_sv_verify():
+    dev = torch.device("cuda")
+    w = synth.c2(seed=7, device=dev)
+    B, K, V = w.B, w.K, w.V
+    lin = binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, 11)
+    N = K + 1
+    draft = torch.cat([w.draft, torch.zeros((B, 1, V), dtype=w.draft.dtype, device=dev)], dim=1).contiguous()
+    toks = torch.cat([torch.zeros((B, 1), dtype=torch.int32, device=dev), w.draft_tokens], dim=1).contiguous()
+    par = torch.arange(-1, K, dtype=torch.int32, device=dev).repeat(B, 1).contiguous()
+    tr = binding.verify_tree(w.target, draft, toks, par, w.temperature, 11)
+    same = (tr["accept_len"] == lin["accept_len"]) & torch.all(tr["tokens"] == lin["tokens"], dim=1)
+    # both are fp32 paths of the same rule; only draws within rounding of a
+    # boundary may differ
+    assert same.float().mean() > 0.97, same.float().mean()
+
+
+def test_tree_greedy_by_hand_and_bad_trees():
+    dev = torch.device("cuda")
+    V, N = 4, 6
+    par = torch.tensor([[-1, 0, 0, 1, 2, 2], [-1, 0, 0, 1, 2, 2], [-1, 0, 3, 1, 2, 2]], dtype=torch.int32)
+    tok = torch.tensor([[0, 2, 3, 0, 1, 3]] * 3, dtype=torch.int32)
+    t = torch.zeros((3, N, V))
+    t[:, 0, 3] = 5.0
+    t[:, 2, 3] = 5.0
+    t[:, 5, 1] = 5.0
+    t[1, 2, 3], t[1, 2, 0] = 0.0, 5.0
+    out = binding.verify_tree(t.to(dev), torch.zeros_like(t).to(dev), tok.to(dev), par.to(dev),
+                              torch.zeros(3, device=dev), 0)
+    o = {k: v.cpu().numpy() for k, v in out.items()}
+    assert list(o["tokens"][0]) == [3, 3, 1, -1, -1, -1] and o["accept_len"][0] == 2
+    assert list(o["path"][0][:2]) == [2, 5]
+    assert list(o["tokens"][1][:3]) == [3, 0, -1] and o["accept_len"][1] == 1
+    assert o["flags"][2] == 2 and o["accept_len"][2] == 0 and (o["tokens"][2] == -1).all()
