@@ -398,6 +398,165 @@ def run_reference(args):
     print(json.dumps(res), flush=True)
 
 
+# --------------------------------------------------------------------------- the steps around verification
+OPS = {
+    "budget": "AV global budget: B=512 K=16 confidences (Beta, mean 0.88-0.035i), synthetic cost tables",
+    "post": "post-verify update: B=1024 K=7, ragged draft lengths, history capacity 4096",
+    "tts": "TTS signal: B=256 K=5 V=128256 bf16 (the c3 rows), weights 0.9^k, KL + bf16 gradient",
+    "tree": "tree acceptance: B=256 V=32000 bf16, 16-node trees (levels 3,6,4,2), tau~U(0.4,1.3), 10% greedy",
+}
+
+
+def _flush_l2(buf):
+    buf.add_(1)  # 256 MB written: evicts the 129 MB L2
+
+
+def run_op(args):
+    """Times one of the steps around verification (single GPU) and prints one
+    JSON line in the same format as the main benchmark."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_verification_03_gb300 import binding, synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    binding.lib()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
+    op = args.op
+    if op == "budget":
+        B, K = 512, 16
+        conf, dc, vc = (t.to(dev) for t in synth.budget_inputs(B, K, seed=0))
+        out_b = torch.empty(1, dtype=torch.int32, device=dev)
+        out_k = torch.empty(B, dtype=torch.int32, device=dev)
+        call = lambda i: binding.av_budget(conf, B, dc, vc, out_budget=out_b, out_kept_len=out_k)
+        units, unit = B * K, "drafts ranked/s"
+        nbytes = B * K * 4 + 2 * (B * K + 1) * 4 + B * 4 + 4
+    elif op == "post":
+        B, K, H = 1024, 7, 4096
+        rng = np.random.default_rng(0)
+        kl = rng.integers(0, K + 1, B).astype(np.int32)
+        acc = np.array([rng.integers(0, k + 1) for k in kl], np.int32)
+        outs = np.full((B, K + 1), -1, np.int32)
+        for b in range(B):
+            outs[b, :acc[b] + 1] = rng.integers(0, 150000, acc[b] + 1)
+        T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        ins, o, a, dl = T(rng.integers(0, 150000, (B, K + 1)).astype(np.int32)), T(outs), T(acc), T(kl)
+        sl0 = T(rng.integers(0, H // 2, B).astype(np.int32))
+        sl, kv = sl0.clone(), sl0.clone()
+        hist = torch.zeros((B, H), dtype=torch.int32, device=dev)
+        nxt = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        fl = torch.empty(B, dtype=torch.int32, device=dev)
+
+        def reset():
+            sl.copy_(sl0)
+            kv.copy_(sl0)
+
+        def call(i):
+            binding.post_verify(ins, o, a, sl, kv, history=hist, draft_len=dl, next_in=nxt, flags=fl)
+        units, unit = B, "sequences/s"
+        nbytes = B * (4 * (K + 1) * 3 + 4 * 5) + int((acc + 1).sum()) * 4
+    elif op == "tts":
+        w = synth.c3(seed=0, device=dev)
+        B, K, V = w.B, w.K, w.V
+        wt = torch.tensor([0.9 ** k for k in range(K)], dtype=torch.float32, device=dev)
+        kl_out = torch.empty((B, K), dtype=torch.float32, device=dev)
+        grad = torch.empty((B, K, V), dtype=torch.bfloat16, device=dev)
+        call = lambda i: binding.tts_signal(w.target, w.draft, w.temperature, wt, out_kl=kl_out, out_grad=grad)
+        units, unit = B * K, "canvas positions/s"
+        nbytes = B * K * V * 2 * 3 + B * K * 4  # both rows read once, the gradient written once
+    elif op == "tree":
+        w = synth.tree(seed=0, B=256, V=32000, device=dev)
+        B, N, V = w.B, w.N, w.V
+        res = {}
+
+        def call(i):
+            res["out"] = binding.verify_tree(w.target, w.draft, w.tokens, w.parents, w.temperature, i)
+        units, unit = B, "requests/s"
+        nbytes = None  # from the walked paths below
+    else:
+        raise SystemExit("unknown op " + op)
+
+    for i in range(args.warmup):
+        call(10**6 + i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = Clocks(0)
+    time.sleep(0.3)
+    visited = 0
+    for i in range(args.steps):
+        _flush_l2(flush)
+        if op == "post":
+            reset()  # lengths back to the start state, outside the timed launch
+        ev[i][0].record(stream)
+        call(i)
+        ev[i][1].record(stream)
+        if op == "tree":
+            visited += int((res["out"]["accept_len"] + 1).sum().item()) if i == 0 else 0
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)
+    mean_ms = sum(ms) / len(ms)
+    if op == "tree":
+        nbytes = visited * 2 * V * 2  # each visited node's target and draft rows, read once
+    value = units / (mean_ms / 1e3)
+    peak, kind = _peak()
+    achieved = nbytes / (mean_ms / 1e3) / 1e9
+    kernel = dict(budget="av_budget_kernel", post="post_verify_kernel", tts="tts_kernel", tree="tree_kernel")[op]
+    res_line = dict(metric=unit.replace("/s", " per second") + " (" + op + ")", value=value, unit=unit, n_gpus=1,
+                    steps=args.steps, warmup=args.warmup, ms_per_step=mean_ms, higher_is_better=True,
+                    scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
+                    ms_p10_p50_p90=[ms[len(ms) // 10], ms[len(ms) // 2], ms[(9 * len(ms)) // 10]],
+                    roofline=dict(bound="hbm", kernel=kernel, achieved=achieved, peak=peak, unit="GB/s",
+                                  frac=achieved / peak, traffic=None, algorithmic_bytes_per_launch=nbytes,
+                                  peak_source="%s (MEASURED_PEAKS hbm_gbs)" % kind if kind == "measured"
+                                  else "fallback 6.8 TB/s"),
+                    gpu_launches=args.steps, clocks=clk,
+                    config=dict(workload=op + ": " + OPS[op], l2="256 MB written between timed launches",
+                                timing="CUDA events around each launch"))
+    if not args.no_cpu:
+        res_line["cpu_baseline"] = _op_cpu_baseline(op)
+    print(json.dumps(res_line), flush=True)
+
+
+def _op_cpu_baseline(op):
+    """The oracle on a bounded sample of the same workload (one host core)."""
+    import numpy as np
+
+    import oracle
+    from speculative_decoding_verification_03_gb300 import synth
+
+    t0 = time.perf_counter()
+    if op == "budget":
+        conf, dc, vc = synth.budget_inputs(512, 16, seed=0)
+        oracle.av_budget(conf.numpy(), 512, dc.numpy(), vc.numpy())
+        units, unit, sample = 512 * 16, "drafts ranked/s", "one call, B=512 K=16"
+    elif op == "post":
+        rng = np.random.default_rng(0)
+        B, K = 1024, 7
+        kl = rng.integers(0, K + 1, B)
+        acc = np.array([rng.integers(0, k + 1) for k in kl])
+        outs = np.full((B, K + 1), 5, np.int32)
+        oracle.post_verify(np.zeros((B, K + 1), np.int32), outs, acc, np.zeros(B), np.zeros(B),
+                           np.zeros((B, 64), np.int32), draft_len=kl)
+        units, unit, sample = B, "sequences/s", "one call, B=1024 K=7"
+    elif op == "tts":
+        w = synth.c3(seed=0, B=8)
+        t = (synth.logits_np(w.target).astype(np.uint32) << 16).view(np.float32)
+        d = (synth.logits_np(w.draft).astype(np.uint32) << 16).view(np.float32)
+        oracle.tts_signal(t, d, w.temperature.numpy(), [0.9 ** k for k in range(w.K)])
+        units, unit, sample = 8 * w.K, "canvas positions/s", "8 requests of the c3 rows"
+    else:
+        w = synth.tree(seed=0, B=8, V=32000)
+        T = (synth.logits_np(w.target).astype(np.uint32) << 16).view(np.float32)
+        D = (synth.logits_np(w.draft).astype(np.uint32) << 16).view(np.float32)
+        oracle.verify_tree(T, D, w.tokens.numpy(), w.parents.numpy(), w.temperature.numpy(), 0)
+        units, unit, sample = 8, "requests/s", "8 requests of the tree workload"
+    dt = time.perf_counter() - t0
+    return dict(value=units / dt, unit=unit, cores=1, kind="oracle", sample=sample)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -408,9 +567,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--op", choices=["verify"] + sorted(OPS), default="verify",
+                    help="verify (the hot path, default) or one of the steps around it")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.op != "verify":
+        if args.impl == "reference" or args.gpus != 1:
+            raise SystemExit("--op other than verify runs on one GPU, GB300 arm only")
+        run_op(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
