@@ -134,6 +134,22 @@ def _dist():
     return ws, rank, local
 
 
+def _aggregate(elapsed_ms: float, units: float, device):
+    """Whole-job timing over the ranks of the default process group: the
+    slowest rank's elapsed time (max) and the units all ranks processed
+    (sum).  With one process it returns its arguments."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(elapsed_ms), float(units)
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def _bytes_per_step(wl, K, V, esz, kept, accept):
     """Algorithmic bytes of one step.  Returns (bytes of the verify row-pass
     launch that the launch events bracket, all bytes of the step).  The step
@@ -236,12 +252,6 @@ def run_gpu(args):
     rc, flags = binding.status(ws)
     if rc != 0:
         raise SystemExit("device status %d (flags %#x) in the timed region" % (rc, flags))
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
-
     # work done: verified rows (sum over sequences of k_b + 1) and algorithmic bytes
     esz = w.target.element_size()
     rows, bytes_rp, bytes_all = 0, 0, 0
@@ -252,7 +262,8 @@ def run_gpu(args):
         rows += int((k + 1).sum())
         bytes_rp += f
         bytes_all += t
-    value = rows * world / (elapsed_ms / 1e3)
+    elapsed_ms, rows_all = _aggregate(elapsed_ms, rows, dev)  # max time, summed rows over ranks
+    value = rows_all / (elapsed_ms / 1e3)
     # one launch of the row-pass kernel per step (verification, sampling and
     # the refit fused), plus the AV scoring row pass on the truncated canvas;
     # the workspace memset is a driver fill, not a kernel
