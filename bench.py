@@ -152,25 +152,29 @@ def _aggregate(elapsed_ms: float, units: float, device):
 
 def _bytes_per_step(wl, K, V, esz, kept, accept):
     """Algorithmic bytes of one step.  Returns (bytes of the verify row-pass
-    launch that the launch events bracket, all bytes of the step).  The step
-    reads every verified target row (k_b + 1) and draft row (k_b) once,
-    re-reads the residual or bonus target row (+ the draft row when
-    rejected), and moves 4 B (3K + 4) of small per-sequence inputs and
-    outputs.  On the AV-truncated canvas the scoring call reads all K draft
-    rows, and the verify row pass then reads only the k_b + 1 target rows
-    (plus the second pass)."""
+    launch that the launch events bracket, all bytes of the step).  The
+    acceptance walk needs target rows 0 .. a_b only (the row after the last
+    accepted draft; nothing past the first rejection is read) and every
+    verified draft row (k_b of them: they carry the AV scores); the second
+    pass re-reads the residual or bonus target row (+ the draft row when
+    rejected); 4 B (3K + 4) of small per-sequence inputs and outputs.  On the
+    AV-truncated canvas the scoring call reads all K draft rows and the verify
+    row pass only target rows (plus the second pass).  The eager count (every
+    verified target row k_b + 1) is returned as well, for comparison."""
     B = kept.size
     second = int(B + (accept < kept).sum()) * V * esz
     small = 4 * B * (3 * K + 4)
+    targets = int((accept + 1).sum()) * V * esz
     if wl == "c5":
-        verify_first = int((kept + 1).sum()) * V * esz
+        verify_first = targets
         first = verify_first + B * K * V * esz
     else:
-        verify_first = first = int((2 * kept + 1).sum()) * V * esz
+        verify_first = first = targets + int(kept.sum()) * V * esz
     # the bracketed verify row pass also samples (second-pass rows) when the
     # rows are 16-byte aligned, as on every workload here
     bracketed = verify_first + second + small
-    return bracketed, first + second + small
+    eager = (int((kept + 1).sum()) + (0 if wl == "c5" else int(kept.sum()))) * V * esz + second + small
+    return bracketed, first + second + small, eager
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -254,14 +258,15 @@ def run_gpu(args):
         raise SystemExit("device status %d (flags %#x) in the timed region" % (rc, flags))
     # work done: verified rows (sum over sequences of k_b + 1) and algorithmic bytes
     esz = w.target.element_size()
-    rows, bytes_rp, bytes_all = 0, 0, 0
+    rows, bytes_rp, bytes_all, bytes_eager = 0, 0, 0, 0
     for acc, kept in outcomes:
         a = acc.cpu().numpy()
         k = np.full(B, K) if kept is None else kept.cpu().numpy()
-        f, t = _bytes_per_step(args.workload, K, V, esz, k, a)
+        f, t, e = _bytes_per_step(args.workload, K, V, esz, k, a)
         rows += int((k + 1).sum())
         bytes_rp += f
         bytes_all += t
+        bytes_eager += e
     elapsed_ms, rows_all = _aggregate(elapsed_ms, rows, dev)  # max time, summed rows over ranks
     value = rows_all / (elapsed_ms / 1e3)
     # one launch of the row-pass kernel per step (verification, sampling and
@@ -282,7 +287,11 @@ def run_gpu(args):
                            frac=achieved / peak, peak_source="%s (MEASURED_PEAKS hbm_gbs)" % peak_kind
                            if peak_kind == "measured" else "fallback 6.8 TB/s",
                            traffic=_traffic(args.workload), algorithmic_bytes_per_launch=rp_bytes,
-                           ms_per_launch=rp_ms)
+                           ms_per_launch=rp_ms,
+                           # the same launch counted with every verified target row read
+                           # (the definition without early exit), for comparison
+                           eager_bytes_per_launch=bytes_eager / args.steps,
+                           frac_eager_bytes=bytes_eager / args.steps / (rp_ms / 1e3) / 1e9 / peak)
     res["step_hbm"] = dict(algorithmic_bytes_per_step=bytes_all / args.steps,
                            achieved_gbs=bytes_all / args.steps / (elapsed_ms / args.steps / 1e3) / 1e9)
     res["gpu_launches"] = launches_per_step * args.steps

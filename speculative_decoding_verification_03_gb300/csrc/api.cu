@@ -208,20 +208,31 @@ sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *targe
   // separate sampler kernel follows the row pass.
   P.nstatic = P.nitems;
   P.fused = ((size_t)V * esz) % 16 == 0 && aligned(target_logits, 16) && (!draft_logits || aligned(draft_logits, 16));
+  size_t clear = L.counters_off + L.counters_bytes;
   if (P.fused) {
     int sp = (S.nsub + 127) / 128;
     sp = sp < 1 ? 1 : (sp > kMaxSampleParts ? kMaxSampleParts : sp);
     P.sp = sp;
     P.spc = (S.nsub + sp - 1) / sp;
-    P.ndyn = B * sp;
     P.dq = reinterpret_cast<int *>(w + L.dq_off);
     P.dq_tail = P.ticket + 1;
     P.dq_head = P.ticket + 2;
     P.smp = S;
+    // early exit: target rows past a sequence's first rejection are not read
+    P.lazy = 1;
+    P.ngroups = P.mode == kVerifyFull ? K + 1 : 1;
+    P.nstatic = P.nitems = P.ngroups * B * P.nch;
+    // queued target rows stay whole: measured, chunking them only adds
+    // per-chunk merge work to the chain of decisions
+    P.nch_dyn = 1;
+    P.chunk_elems_dyn = (V + kChunkAlignElems - 1) / kChunkAlignElems * kChunkAlignElems;
+    P.ndyn = B * (sp + K * P.nch_dyn);
+    P.pos_cnt = reinterpret_cast<uint32_t *>(w + L.pos_cnt_off);
+    clear = L.dq_off + (size_t)P.ndyn * 4;
   }
 
   // status word (offset 0) and the per-call counters, in one clear
-  cudaError_t e = cudaMemsetAsync(w, 0, L.counters_off + L.counters_bytes, st);
+  cudaError_t e = cudaMemsetAsync(w, 0, clear, st);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   const long long tickets = (long long)P.nitems + (P.fused ? P.ndyn : 0);
   const int grid = tickets < sms ? (int)tickets : sms;

@@ -625,6 +625,213 @@ __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Early exit: the acceptance walk one position at a time, as the rows of that
+// position finish (fused verify modes).
+// ---------------------------------------------------------------------------
+
+// fp32 acceptance test of position i with the exact fp64 fallback (one lane).
+__device__ __forceinline__ bool reject_at(const RowPassParams &P, int b, int i, const Part &T, const Part &D,
+                                          float tau_f, bool greedy, int d, bool in_range) {
+  if (greedy) return !(in_range && d == T.arg);
+  if (!in_range) return true;
+  const float inv_f = 1.f / tau_f;
+  const float u = uniform24f(P.seed, (uint32_t)b, (uint32_t)i, 0);
+  const long long rowb = (long long)P.V;
+  const float zt = logit_at(P.target, P.dtype, ((long long)b * (P.K + 1) + i) * rowb + d);
+  const float zd = logit_at(P.draft, P.dtype, ((long long)b * P.K + i) * rowb + d);
+  const float lnSt = log1pf(T.E), lnSd = log1pf(D.E);
+  const float A = (zt - T.m) * inv_f, Bq = (zd - D.m) * inv_f;
+  const float dl = (A - lnSt) - (Bq - lnSd);
+  const float lu = logf(u);
+  const float band = 2e-6f + 4e-7f * (fabsf(A) + fabsf(Bq) + lnSt + lnSd + fabsf(lu));
+  if (u != 0.f && fabsf(dl - lu) > band) return !(lu < dl);
+  return reject_fp64(zt, zd, T, D, 1.0 / (double)tau_f, (double)u);
+}
+
+// AV feature and confidence of a draft row (fp32, as in finish_verify).
+__device__ __forceinline__ float av_feature(float E) {
+  float x = E > 0.f ? -logf(E) : 30.f;
+  return x > 30.f ? 30.f : (x < -30.f ? -30.f : x);
+}
+__device__ __forceinline__ float av_conf(const RowPassParams &P, int i, float x) {
+  return 1.0f / (1.0f + expf(-fmaf(__ldcg(P.theta), x, __ldcg(P.theta + 1 + i))));
+}
+
+// One label's refit terms as 2^-32 fixed point (one lane).
+__device__ __forceinline__ void fit_label(const RowPassParams &P, int i, float x, float conf, bool accepted) {
+  const float y = accepted ? 1.0f : 0.0f;
+  const float r = conf - y, w = conf * (1.0f - conf);
+  const float q[kFitQ] = {r * x, w * x * x, r, w * x, w, 1.0f};
+#pragma unroll
+  for (int j = 0; j < kFitQ; ++j) atomicAdd(P.fitacc + i * kFitQ + j, (unsigned long long)fixed_2p32(q[j]));
+}
+
+// A sequence finished one of its theta-reading events (a draft row's score,
+// or the final decision).  The event that completes the last sequence of the
+// launch runs the refit round update (warp-wide).
+__device__ void seq_event(const RowPassParams &P, int b, int k, int lane) {
+  const int need = (P.mode == kVerifyFull ? k : 0) + 1;
+  int last = 0;
+  if (lane == 0) {
+    __threadfence();
+    const bool done = atomicAdd(P.seq_cnt + b, 1u) == (uint32_t)need - 1u;
+    if (done && P.fit) last = atomicAdd(P.scans_done, 1u) == (uint32_t)P.B - 1u;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) {
+    __threadfence();
+    double t[kFitQ] = {0, 0, 0, 0, 0, 0};
+    if (lane < P.K) {
+#pragma unroll
+      for (int j = 0; j < kFitQ; ++j)
+        t[j] = (double)(long long)__ldcg(P.fitacc + lane * kFitQ + j) * (1.0 / kFitFixedScale);
+    }
+    av_round_update(P.av_state, P.theta_rw, P.K, P.round_len, P.damping_c, t, lane);
+  }
+}
+
+// The walk ended at position a (a < k: first rejection; a == k: all
+// accepted, bonus): tokens after a, the sampling task and its queue entries
+// (plus fillers for the target rows never queued), the remaining outputs.
+__device__ void lazy_finalize(const RowPassParams &P, int b, int a, int k, int lane) {
+  const int K = P.K;
+  const float tau_f = __ldg(P.temperature + b);
+  const bool greedy = !(tau_f > 0.f);
+  const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
+  uint32_t flags = 0;
+  if (lane == 0) {
+    if (!(tau_f >= 0.f)) flags |= SV_FLAG_BAD_TEMP;
+    if (P.draft_len) {
+      const int kr = __ldg(P.draft_len + b);
+      if (kr < 0 || kr > K) flags |= SV_FLAG_BAD_LEN;
+    }
+  }
+  if (lane < k) {  // every verified draft token is range-checked, as in the full scan
+    const int d = __ldg(P.draft_tokens + (size_t)b * K + lane);
+    if (d < 0 || d >= P.V) flags |= SV_FLAG_TOKEN_RANGE;
+  }
+  // outputs of the positions the walk did not use
+  if (lane < K) {
+    const float nan = __int_as_float(0x7fc00000);
+    if (lane >= k) {
+      if (P.out_feature) P.out_feature[(size_t)b * K + lane] = nan;
+      if (P.out_conf) P.out_conf[(size_t)b * K + lane] = nan;
+    } else if (P.mode == kVerifyTargets && (P.out_feature || P.out_conf)) {
+      const Part D = load_stats_cg(P.draft_stats_in + (size_t)b * K + lane);
+      const float x = av_feature(D.E);
+      if (P.out_feature) P.out_feature[(size_t)b * K + lane] = x;
+      if (P.out_conf) P.out_conf[(size_t)b * K + lane] = av_conf(P, lane, x);
+    }
+  }
+  if (lane <= K && lane > a) P.out_tokens[(size_t)b * (K + 1) + lane] = -1;
+  if (lane == 0) {
+    const Part T = load_stats_cg(st + 2 * a);
+    Part D;
+    D.m = 0.f;
+    D.E = 0.f;
+    if (a < k) D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + a) : load_stats_cg(st + 2 * a + 1);
+    const int argmax_t = (T.arg >= 0 && T.arg < P.V) ? T.arg : 0;
+    if (greedy) P.out_tokens[(size_t)b * (K + 1) + a] = argmax_t;
+    SampleTask t;
+    t.kind = greedy ? kTaskNone : (a < k ? kTaskResidual : kTaskBonus);
+    t.a = a;
+    t.argmax_t = argmax_t;
+    const float inv_f = greedy ? 1.f : 1.f / tau_f;
+    const float c_f = greedy ? kLog2e : kLog2e / tau_f;
+    t.c = c_f;
+    t.invtau = inv_f;
+    t.nbt = -fmaf(T.m, c_f, log1pf(T.E) * kLog2e);
+    t.k0_hi = 0.f;
+    t.k0_lo = 0.f;
+    if (t.kind == kTaskResidual) {
+      const double lnr = log1p(((double)T.E - (double)D.E) / (1.0 + (double)D.E));
+      const double k0 = ((double)T.m - (double)D.m) / (double)tau_f + lnr;
+      t.k0_hi = (float)k0;
+      t.k0_lo = (float)(k0 - (double)t.k0_hi);
+    }
+    t.u = greedy ? 0.0 : (double)uniform24f(P.seed, (uint32_t)b, (uint32_t)a, 1);
+    P.tasks[b] = t;
+    // the sample items (the task is visible first), then fillers for the
+    // target rows K - a that were never queued
+    __threadfence();
+    const int nfill = (K - a) * P.nch_dyn;
+    const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)(P.sp + nfill));
+    for (int q = 0; q < P.sp; ++q) st_relaxed_gpu(P.dq + base + q, b * P.sp + q + 1);
+    for (int q = 0; q < nfill; ++q) st_relaxed_gpu(P.dq + base + P.sp + q, kQueueNop);
+    P.out_accept_len[b] = a;
+  }
+  flags = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && flags) atomicOr(P.status, flags);
+  seq_event(P, b, k, lane);
+}
+
+// Position i (< k) has both rows: test it; accept -> queue target row i + 1,
+// reject -> finalize.
+__device__ void lazy_decide(const RowPassParams &P, int b, int i, int k, int lane) {
+  const int K = P.K;
+  int rej = 0;
+  if (lane == 0) {
+    const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
+    const Part T = load_stats_cg(st + 2 * i);
+    const Part D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + i) : load_stats_cg(st + 2 * i + 1);
+    const float tau_f = __ldg(P.temperature + b);
+    const bool greedy = !(tau_f > 0.f);
+    const int d = __ldg(P.draft_tokens + (size_t)b * K + i);
+    const bool in_range = d >= 0 && d < P.V;
+    const bool reject = reject_at(P, b, i, T, D, tau_f, greedy, d, in_range);
+    if (!reject) {
+      // queue target row i + 1 first: it is on the sequence's critical path
+      const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)P.nch_dyn);
+      const int code0 = P.B * P.sp + (b * K + i) * P.nch_dyn + 1;
+      for (int c = 0; c < P.nch_dyn; ++c) st_relaxed_gpu(P.dq + base + c, code0 + c);
+      P.out_tokens[(size_t)b * (K + 1) + i] = d;
+    }
+    if (P.fit) {
+      const float x = av_feature(D.E);
+      fit_label(P, i, x, av_conf(P, i, x), !reject);
+    }
+    rej = reject;
+  }
+  rej = __shfl_sync(0xffffffffu, rej, 0);
+  if (rej) lazy_finalize(P, b, i, k, lane);
+}
+
+// A row of sequence b finished (sidx = 2 i: target row i, 2 i + 1: draft row i).
+__device__ __noinline__ void lazy_row_done(const RowPassParams &P, int b, int sidx, int lane) {
+  const int k = kept_len_of(P, b);
+  const int i = sidx >> 1;
+  if (sidx & 1) {  // draft row i: its score, then position i may be ready
+    int ready = 0;
+    if (lane == 0) {
+      const Part D = load_stats_cg(P.stats + (size_t)b * (2 * P.K + 1) + sidx);
+      if (D.flags & SV_FLAG_NONFINITE) atomicOr(P.status, SV_FLAG_NONFINITE);
+      if (P.out_feature || P.out_conf) {
+        const float x = av_feature(D.E);
+        if (P.out_feature) P.out_feature[(size_t)b * P.K + i] = x;
+        if (P.out_conf) P.out_conf[(size_t)b * P.K + i] = av_conf(P, i, x);
+      }
+      ready = atomicAdd(P.pos_cnt + (size_t)b * (P.K + 1) + i, 1u) == 1u;
+      if (ready) __threadfence();
+    }
+    ready = __shfl_sync(0xffffffffu, ready, 0);
+    if (ready) lazy_decide(P, b, i, k, lane);
+    seq_event(P, b, k, lane);
+    return;
+  }
+  int ready = 0;
+  if (lane == 0) {
+    const Part T = load_stats_cg(P.stats + (size_t)b * (2 * P.K + 1) + sidx);
+    if (T.flags & SV_FLAG_NONFINITE) atomicOr(P.status, SV_FLAG_NONFINITE);
+    ready = (i == k || P.mode == kVerifyTargets) ? 1 : atomicAdd(P.pos_cnt + (size_t)b * (P.K + 1) + i, 1u) == 1u;
+    if (ready) __threadfence();
+  }
+  ready = __shfl_sync(0xffffffffu, ready, 0);
+  if (!ready) return;
+  if (i == k) lazy_finalize(P, b, k, k, lane);  // every draft accepted: bonus from row k
+  else lazy_decide(P, b, i, k, lane);
+}
+
 __device__ void finish_score(const RowPassParams &P, int b, int lane) {
   const int K = P.K;
   const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
@@ -718,6 +925,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
     }
     for (;;) {
       int dyn = -1;
+      int row_b = 0, row_chunk = 0, row_target = 0, row_pos = 0;
       if (dyn_left) {
         if (pending < 0 && (q_head < q_tail || !static_left)) {
           const int c = (int)atomicAdd(P.dq_head, 1u);
@@ -772,7 +980,19 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
             break;
           }
         }
+        if (code == kQueueNop) continue;
         --code;
+        if (code >= P.B * P.sp) {
+          // a queued target row (early exit): (b K + i - 1) nch + chunk
+          const int r = code - P.B * P.sp;
+          row_chunk = r % P.nch_dyn;
+          const int q = r / P.nch_dyn;
+          row_b = q / K;
+          row_pos = q - row_b * K + 1;
+          row_target = 1;
+          goto stage_row;
+        }
+        {
         const int b = code / P.sp, part = code - (code / P.sp) * P.sp;
         const SampleTask t = load_task_cg(P.tasks + b);
         if (t.kind == kTaskNone) continue;
@@ -821,27 +1041,43 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
         }
         if (!ok) break;
         continue;
+        }
       }
-      const int per_seq = P.nslot * P.nch;
-      const int b = item / per_seq;
-      const int rem = item - b * per_seq;
-      const int slot = rem / P.nch;
-      const int chunk = rem - slot * P.nch;
+      if (P.lazy) {
+        // static items, position-major: group 0 = every first target row,
+        // group g >= 1 = every draft row g - 1
+        const int per_group = P.B * P.nch;
+        const int g = item / per_group;
+        const int rem = item - g * per_group;
+        row_b = rem / P.nch;
+        row_chunk = rem - row_b * P.nch;
+        row_target = g == 0;
+        row_pos = g == 0 ? 0 : g - 1;
+      } else {
+        const int per_seq = P.nslot * P.nch;
+        row_b = item / per_seq;
+        const int rem = item - row_b * per_seq;
+        const int slot = rem / P.nch;
+        row_chunk = rem - slot * P.nch;
+        slot_kind(P.mode, K, slot, row_target, row_pos);
+      }
+    stage_row:
+      const int b = row_b, chunk = row_chunk, is_target = row_target, pos = row_pos;
       if (b != cached_b) {
         cached_b = b;
         cached_k = kept_len_of(P, b);
         cached_c = row_scale(P, b);
       }
-      int is_target, pos;
-      slot_kind(P.mode, K, slot, is_target, pos);
       if (P.mode != kScore) {
         if (is_target ? (pos > cached_k) : (pos >= cached_k)) continue;
       }
       const long long row = is_target ? ((long long)b * (K + 1) + pos) : ((long long)b * K + pos);
       const long long row_off = row * (long long)P.V;
       const char *base = reinterpret_cast<const char *>(is_target ? P.target : P.draft);
-      const int e_beg = chunk * P.chunk_elems;
-      const int e_end = min(P.V, e_beg + P.chunk_elems);
+      // queued target rows (early exit) have their own, finer chunks
+      const int celems = (P.lazy && is_target && pos > 0) ? P.chunk_elems_dyn : P.chunk_elems;
+      const int e_beg = chunk * celems;
+      const int e_end = min(P.V, e_beg + celems);
       const uintptr_t a_beg = reinterpret_cast<uintptr_t>(base) + (uintptr_t)(row_off + e_beg) * kEsz;
       const uintptr_t a_end = reinterpret_cast<uintptr_t>(base) + (uintptr_t)(row_off + e_end) * kEsz;
       int a0 = e_beg + (int)(((16 - (a_beg & 15)) & 15) / kEsz);
@@ -977,29 +1213,36 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
       if (lane == 0) {
         const size_t row = (size_t)info.b * (2 * K + 1) + info.sidx;
         bool row_done = true;
-        if (P.nch > 1) {
+        const int nch_row = (P.lazy && !(info.sidx & 1) && info.sidx > 0) ? P.nch_dyn : P.nch;
+        if (nch_row > 1) {
           store_stats(P.chunk_part + row * kMaxChunks + info.chunk, R);
           __threadfence();
           const uint32_t old = atomicAdd(P.row_cnt + row, 1u);
-          row_done = (old == (uint32_t)P.nch - 1u);
+          row_done = (old == (uint32_t)nch_row - 1u);
           if (row_done) {
             __threadfence();
             R = load_stats_cg(P.chunk_part + row * kMaxChunks + 0);
-            for (int c = 1; c < P.nch; ++c) R = combine(R, load_stats_cg(P.chunk_part + row * kMaxChunks + c), info.c);
+            for (int c = 1; c < nch_row; ++c) R = combine(R, load_stats_cg(P.chunk_part + row * kMaxChunks + c), info.c);
           }
         }
         if (row_done) {
           if (R.arg == INT_MAX || !(fabsf(R.m) <= FLT_MAX) || isnan(R.E)) R.flags |= SV_FLAG_NONFINITE;
           store_stats(P.stats + row, R);
           __threadfence();
-          const int k = kept_len_of(P, info.b);
-          const uint32_t old = atomicAdd(P.seq_cnt + info.b, 1u);
-          seq_done = (old == (uint32_t)rows_needed(P, k) - 1u);
-          if (seq_done) __threadfence();
+          if (P.lazy) {
+            seq_done = 2;  // hand the finished row to the walk below
+          } else {
+            const int k = kept_len_of(P, info.b);
+            const uint32_t old = atomicAdd(P.seq_cnt + info.b, 1u);
+            seq_done = (old == (uint32_t)rows_needed(P, k) - 1u);
+            if (seq_done) __threadfence();
+          }
         }
       }
       seq_done = __shfl_sync(0xffffffffu, seq_done, 0);
-      if (seq_done) {
+      if (seq_done == 2) {
+        lazy_row_done(P, info.b, info.sidx, lane);
+      } else if (seq_done) {
         __threadfence();
         if (P.mode == kScore) finish_score(P, info.b, lane);
         else finish_verify(P, info.b, lane);

@@ -39,6 +39,7 @@ constexpr int kSampleUnroll = 4;                   // sub-chunks a warp loads be
 constexpr int kSampleCtasPerSm = 3;                // grid of the grid-stride sampler
 
 enum TaskKind : int { kTaskNone = 0, kTaskResidual = 1, kTaskBonus = 2 };
+constexpr int kQueueNop = 0x7fffffff;
 
 // Everything the sampler needs for sequence b, written by the acceptance scan.
 //   p_v  proportional to 2^(z_t[v] * c + nbt)
@@ -120,6 +121,17 @@ struct RowPassParams {
   unsigned char *av_state;
   unsigned long long *fitacc;  // [SV_MAX_K][kFitQ]
   uint32_t *scans_done;
+  // early exit (fused verify modes): the static items are every sequence's
+  // first target row and its draft rows, position-major (all t0, all d0,
+  // all d1, ...); target row i + 1 of a sequence is queued when position i
+  // is accepted, so no target row past the first rejection is read.  Queue
+  // codes: 1 + b sp + part (sample items), 1 + B sp + (b K + i - 1) nch_dyn + chunk
+  // (target row i), kQueueNop (fillers that keep the queue's length fixed).
+  int lazy;
+  int ngroups;        // static groups: first target rows, then draft rows of each position
+  int nch_dyn;        // chunks of a queued target row (shortens the chain of decisions)
+  int chunk_elems_dyn;
+  uint32_t *pos_cnt;  // [B][K+1]: finished rows of position i
 };
 
 
@@ -128,7 +140,7 @@ constexpr int kMaxSampleParts = 16;
 
 struct WsLayout {
   size_t counters_off, counters_bytes;  // zeroed by every call
-  size_t ticket_off, fitacc_off, row_cnt_off, seq_cnt_off, smp_cnt_off, dq_off;
+  size_t ticket_off, fitacc_off, row_cnt_off, seq_cnt_off, smp_cnt_off, pos_cnt_off, dq_off;
   size_t stats_off, chunk_off, task_off, subsum_off;
   size_t total;
 };
@@ -151,8 +163,10 @@ inline WsLayout ws_layout(int B, int K, int V) {
   off += (size_t)B * 4;
   L.smp_cnt_off = off;
   off += (size_t)B * 4;
-  L.dq_off = off;
-  off += (size_t)B * kMaxSampleParts * 4;
+  L.pos_cnt_off = off;
+  off += (size_t)B * (K + 1) * 4;
+  L.dq_off = off;  // last: a call clears only the entries it uses
+  off += (size_t)B * (kMaxSampleParts + (size_t)K * kMaxChunks) * 4;
   off = align_up(off, 256);
   L.counters_bytes = off - L.counters_off;
   L.stats_off = off;
