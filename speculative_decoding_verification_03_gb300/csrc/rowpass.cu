@@ -909,14 +909,14 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
     float cached_c = 1.f;
     bool ok = true;
     const int K = P.K;
-    // Static row tickets are fetched one item ahead, so the atomic's round
-    // trip overlaps the staging of the current item.  Sample items are
-    // claimed with one atomicAdd each (a unique slot, no retries); a claimed
-    // slot whose entry is not yet published stays pending while row items
-    // continue, and is waited on (bounded) only when no row item is left.
+    // A static ticket is taken only when its item is staged (a ticket held
+    // while queued items go first would delay a row the decisions wait for).
+    // Queued items are claimed with one atomicAdd each (a unique slot, no
+    // retries); a claimed slot whose entry is not yet published stays
+    // pending while static items continue, and is waited on (bounded) only
+    // when no static item is left.
     bool static_left = true, dyn_left = P.fused != 0;
-    int next_static = (int)atomicAdd(P.ticket, 1u);
-    int pending = -1;   // claimed sample slot, not yet taken
+    int pending = -1;   // claimed queue slot, not yet taken
     int pend_val = 0;   // its entry as last read (one item ahead)
     int q_head = 0, q_tail = 0;
     if (P.fused) {
@@ -953,12 +953,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
           if (dyn_left) continue;
           break;
         }
-        item = next_static;
+        item = (int)atomicAdd(P.ticket, 1u);
         if (item >= P.nstatic) {
           static_left = false;
           continue;
         }
-        next_static = (int)atomicAdd(P.ticket, 1u);
       }
       if (item >= P.nstatic) {
         // ---- a sample item: its slot is reserved; wait (bounded) for the entry
@@ -1045,7 +1044,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
       }
       if (P.lazy) {
         // static items, position-major: group 0 = every first target row,
-        // group g >= 1 = every draft row g - 1
+        // group g >= 1 = every draft row g - 1 (measured: pairing each
+        // sequence's target and draft row 0 in one group is slower)
         const int per_group = P.B * P.nch;
         const int g = item / per_group;
         const int rem = item - g * per_group;
