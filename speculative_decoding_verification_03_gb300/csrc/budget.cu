@@ -4,10 +4,12 @@
 // request), estimate the accepted tokens of a budget of n drafts as the
 // number of requests plus the n largest survivals, and keep the n that
 // maximises estimate / (draft cost + verify cost).  One CTA: survivals and
-// 64-bit sort keys in shared memory, a bitonic sort, an fp64 block scan of
-// the ranked survivals, an argmax, and per-request kept counts.
+// 64-bit sort keys in shared memory, a bitonic sort, a double-float block
+// scan of the ranked survivals, an argmax (coarse in fp32, exact in fp64
+// near the maximum), and per-request kept counts.
 #include <cfloat>
 
+#include "sample_common.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -15,6 +17,7 @@ namespace sv {
 namespace {
 
 constexpr int kBudgetThreads = 1024;
+constexpr int kBudgetWarps = kBudgetThreads / 32;
 
 struct BudgetParams {
   int B, K, n_req, npad;
@@ -35,33 +38,27 @@ __device__ __forceinline__ float key_survival(uint64_t key) {
   return __uint_as_float(0xffffffffu - (uint32_t)(key >> 32));
 }
 
-__device__ __forceinline__ double warp_incl_scan_f64(double v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
-}
-
 __global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const BudgetParams P) {
   extern __shared__ uint64_t keys[];
-  __shared__ double s_wsum[kBudgetThreads / 32];
-  __shared__ double s_bratio[kBudgetThreads / 32];
-  __shared__ int s_bn[kBudgetThreads / 32];
+  __shared__ float s_whi[kBudgetWarps], s_wlo[kBudgetWarps], s_bf[kBudgetWarps];
+  __shared__ double s_bratio[kBudgetWarps];
+  __shared__ int s_bn[kBudgetWarps];
   __shared__ int s_ncand;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = P.B, K = P.K, NK = B * K, npad = P.npad;
 
+  float *cf = reinterpret_cast<float *>(keys + npad);  // the confidences, staged
   if (tid == 0) s_ncand = 0;
   for (int b = tid; b < B; b += kBudgetThreads) P.out_kept[b] = 0;
+  for (int j = tid; j < NK; j += kBudgetThreads) cf[j] = __ldg(P.conf + j);  // coalesced
+  __syncthreads();
   // 1. survivals (fp32 running product in position order) and keys
   for (int b = tid; b < B; b += kBudgetThreads) {
     int k = P.draft_len ? __ldg(P.draft_len + b) : K;
     k = k < 0 ? 0 : (k > K ? K : k);
     float run = 1.f;
     for (int i = 0; i < K; ++i) {
-      run = __fmul_rn(run, __ldg(P.conf + (size_t)b * K + i));
+      run = __fmul_rn(run, cf[b * K + i]);
       const bool cand = i < k && !isnan(run);
       keys[b * K + i] = cand ? budget_key(run, b * K + i) : ~0ull;
     }
@@ -69,11 +66,12 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const Budg
   for (int j = NK + tid; j < npad; j += kBudgetThreads) keys[j] = ~0ull;
   __syncthreads();
 
-  // 2. bitonic sort, ascending keys
+  // 2. bitonic sort, ascending keys (strides are powers of two: shifts)
   for (int size = 2; size <= npad; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+    for (int sh = __ffs(size) - 2; sh >= 0; --sh) {
+      const int stride = 1 << sh;
       for (int t = tid; t < (npad >> 1); t += kBudgetThreads) {
-        const int lo = 2 * stride * (t / stride) + (t % stride), hi = lo + stride;
+        const int lo = ((t >> sh) << (sh + 1)) + (t & (stride - 1)), hi = lo + stride;
         const bool up = (lo & size) == 0;
         const uint64_t x = keys[lo], y = keys[hi];
         if ((x > y) == up) {
@@ -91,37 +89,75 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const Budg
   __syncthreads();
   const int N = s_ncand;
 
-  // 4. est[n] = n_req + sum of the n first ranked survivals (fp64): each
-  //    thread a contiguous segment, block scan of the segment sums
+  // 4. est[n] = n_req + sum of the n first ranked survivals, as double-float
+  //    (two fp32 numbers, ~48 bits; fp64 runs at a small fraction of the fp32
+  //    rate on this GPU): each thread a contiguous segment, block scan
   const int per = (N + kBudgetThreads - 1) / kBudgetThreads;
   const int j0 = min(N, tid * per), j1 = min(N, j0 + per);
-  double seg = 0.0;
-  for (int j = j0; j < j1; ++j) seg += (double)key_survival(keys[j]);
-  double incl = warp_incl_scan_f64(seg, lane);
-  if (lane == 31) s_wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const double w = warp_incl_scan_f64(s_wsum[lane], lane);
-    s_wsum[lane] = w;
+  DF seg = {0.f, 0.f};
+  for (int j = j0; j < j1; ++j) seg = df_add_f(seg, key_survival(keys[j]));
+  const DF incl = warp_incl_scan_df(seg, lane);
+  if (lane == 31) {
+    s_whi[warp] = incl.hi;
+    s_wlo[warp] = incl.lo;
   }
   __syncthreads();
-  double run = (double)P.n_req + (warp > 0 ? s_wsum[warp - 1] : 0.0) + (incl - seg);
-  // 5. ratio est[n] / cost[n] and its first maximum over the eligible n
+  if (warp == 0) {
+    const DF w = warp_incl_scan_df(DF{s_whi[lane], s_wlo[lane]}, lane);
+    s_whi[lane] = w.hi;
+    s_wlo[lane] = w.lo;
+  }
+  __syncthreads();
+  DF start = DF{(float)P.n_req, 0.f};  // exact for n_req < 2^24
+  if (warp > 0) start = df_add(start, DF{s_whi[warp - 1], s_wlo[warp - 1]});
+  start = df_add(start, df_add(incl, DF{-seg.hi, -seg.lo}));  // + this warp's exclusive prefix
+
+  // 5. the first n maximising est[n] / cost[n] over the n with cost > 0:
+  //    a coarse fp32 maximum first, then every n within rounding of it
+  //    compared exactly in fp64 (a handful of divisions instead of N)
+  float bestf = -FLT_MAX;
+  {
+    DF run = start;
+    if (tid == 0) {
+      const float cf = __ldg(P.draft_cost) + __ldg(P.verify_cost);
+      if (cf > 0.f && isfinite((float)P.n_req / cf)) bestf = (float)P.n_req / cf;
+    }
+    for (int j = j0; j < j1; ++j) {
+      run = df_add_f(run, key_survival(keys[j]));
+      const float cf = __ldg(P.draft_cost + j + 1) + __ldg(P.verify_cost + j + 1);
+      const float r = run.hi / cf;
+      if (cf > 0.f && isfinite(r) && r > bestf) bestf = r;
+    }
+  }
+  bestf = warp_max(bestf);
+  if (lane == 0) s_bf[warp] = bestf;
+  __syncthreads();
+  bestf = s_bf[0];
+  for (int w = 1; w < kBudgetWarps; ++w) bestf = fmaxf(bestf, s_bf[w]);
+  const float thr = bestf - fabsf(bestf) * 1e-6f;  // fp32 ratios are within ~3 ulps
   double best = -DBL_MAX;
   int bn = INT_MAX;
-  auto consider = [&](int n, double est) {
+  auto consider = [&](int n, const DF &est, float rf) {
+    if (!(rf >= thr)) return;
     const double cost = (double)__ldg(P.draft_cost + n) + (double)__ldg(P.verify_cost + n);
     if (!(cost > 0.0)) return;
-    const double r = est / cost;
-    if (isfinite(r) && r > best) {
+    const double r = ((double)est.hi + (double)est.lo) / cost;
+    if (isfinite(r) && (r > best || (r == best && n < bn))) {
       best = r;
       bn = n;
     }
   };
-  if (tid == 0) consider(0, (double)P.n_req);
-  for (int j = j0; j < j1; ++j) {
-    run += (double)key_survival(keys[j]);
-    consider(j + 1, run);
+  {
+    DF run = start;
+    if (tid == 0) {
+      const float cf = __ldg(P.draft_cost) + __ldg(P.verify_cost);
+      consider(0, DF{(float)P.n_req, 0.f}, (float)P.n_req / cf);
+    }
+    for (int j = j0; j < j1; ++j) {
+      run = df_add_f(run, key_survival(keys[j]));
+      const float cf = __ldg(P.draft_cost + j + 1) + __ldg(P.verify_cost + j + 1);
+      consider(j + 1, run, run.hi / cf);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -138,8 +174,8 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const Budg
   }
   __syncthreads();
   if (warp == 0) {
-    best = s_bratio[lane];
-    bn = s_bn[lane];
+    best = lane < kBudgetWarps ? s_bratio[lane] : -DBL_MAX;
+    bn = lane < kBudgetWarps ? s_bn[lane] : INT_MAX;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const double ob = __shfl_xor_sync(0xffffffffu, best, o);
@@ -176,9 +212,9 @@ extern "C" sv_status_t sv_av_budget(int B, int K, const float *conf, const int32
   if (ds != SV_OK) return ds;
   int npad = 2;
   while (npad < B * K) npad <<= 1;
-  const size_t smem = (size_t)npad * sizeof(uint64_t);
+  const size_t smem = (size_t)npad * sizeof(uint64_t) + (size_t)B * K * sizeof(float);
   const cudaError_t e = cudaFuncSetAttribute(av_budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(SV_BUDGET_MAX * sizeof(uint64_t)));
+                                             (int)(SV_BUDGET_MAX * (sizeof(uint64_t) + sizeof(float))));
   if (e != cudaSuccess) return SV_ERR_CUDA;
   BudgetParams P{B, K, n_req, npad, conf, draft_len, draft_cost, verify_cost, out_budget, out_kept_len};
   av_budget_kernel<<<1, kBudgetThreads, smem, static_cast<cudaStream_t>(stream)>>>(P);

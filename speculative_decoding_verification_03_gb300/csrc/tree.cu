@@ -42,6 +42,27 @@ __device__ __forceinline__ float logit(const void *row, int dtype, int v) {
   return __ldcg(reinterpret_cast<const float *>(row) + v);
 }
 
+// Eight consecutive logits v .. v+7 (v a multiple of 8) of a row: one or two
+// 16-byte loads when the row is 16-byte aligned, else plain loads; tokens at
+// or beyond V read as -inf.
+__device__ __forceinline__ void load8(const void *row, int dtype, int V, int v, bool vec, float (&z)[8]) {
+  if (vec && v + 8 <= V) {
+    if (dtype == SV_BF16) {
+      const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(row) + (v >> 3));
+      z[0] = bf16lo(w.x); z[1] = bf16hi(w.x); z[2] = bf16lo(w.y); z[3] = bf16hi(w.y);
+      z[4] = bf16lo(w.z); z[5] = bf16hi(w.z); z[6] = bf16lo(w.w); z[7] = bf16hi(w.w);
+    } else {
+      const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(row) + (v >> 2));
+      const uint4 b = __ldcg(reinterpret_cast<const uint4 *>(row) + (v >> 2) + 1);
+      z[0] = __uint_as_float(a.x); z[1] = __uint_as_float(a.y); z[2] = __uint_as_float(a.z); z[3] = __uint_as_float(a.w);
+      z[4] = __uint_as_float(b.x); z[5] = __uint_as_float(b.y); z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) z[e] = v + e < V ? logit(row, dtype, v + e) : -INFINITY;
+  }
+}
+
 struct Online {
   float m, s;
 };
@@ -71,12 +92,15 @@ struct NodeDist {
   // residual chain: p_0 = p; p_{j+1} = max(p_j - q, 0) * invR[j]
   int nrej;
   float invR[kTreeMaxChildren];
-  __device__ __forceinline__ float p0(int v) const { return ex2_approx((logit(trow, dtype, v) - Mt) * c) * inv_St; }
-  __device__ __forceinline__ float q(int v) const { return ex2_approx((logit(drow, dtype, v) - Md) * c) * inv_Sd; }
+  __device__ __forceinline__ float p0z(float zt) const { return ex2_approx((zt - Mt) * c) * inv_St; }
+  __device__ __forceinline__ float qz(float zd) const { return ex2_approx((zd - Md) * c) * inv_Sd; }
+  __device__ __forceinline__ float p0(int v) const { return p0z(logit(trow, dtype, v)); }
+  __device__ __forceinline__ float q(int v) const { return qz(logit(drow, dtype, v)); }
   // p_j(v) for j = nrej (the current residual) and the un-normalised
   // max(p_j - q, 0) for the next step
-  __device__ __forceinline__ float pj(int v, float qv) const {
-    float r = p0(v);
+  __device__ __forceinline__ float pj(int v, float qv) const { return pjz(logit(trow, dtype, v), qv); }
+  __device__ __forceinline__ float pjz(float zt, float qv) const {
+    float r = p0z(zt);
     for (int i = 0; i < nrej; ++i) r = fmaxf(r - qv, 0.f) * invR[i];
     return r;
   }
@@ -155,17 +179,22 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       const int nk = s_nkids;
       const void *trow = reinterpret_cast<const char *>(P.target) + ((size_t)b * N + cur) * (size_t)V * esz;
       const void *drow = reinterpret_cast<const char *>(P.draft) + ((size_t)b * N + cur) * (size_t)V * esz;
+      const bool vec = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(drow)) & 15) == 0;
+      const int noct = (V + 7) >> 3;  // groups of 8 consecutive tokens
       int next = -1;
       if (greedy) {
         // argmax of target row cur (lowest index on ties)
         float bv = -INFINITY;
         int bi = INT_MAX;
-        for (int v = tid; v < V; v += kTreeThreads) {
-          const float z = logit(trow, P.dtype, v);
-          if (z > bv) {
-            bv = z;
-            bi = v;
-          }
+        for (int o = tid; o < noct; o += kTreeThreads) {
+          float z[8];
+          load8(trow, P.dtype, V, o << 3, vec, z);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (z[e] > bv) {
+              bv = z[e];
+              bi = (o << 3) + e;
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -205,9 +234,15 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       } else {
         // statistics of both rows
         Online ot = {-INFINITY, 0.f}, od = {-INFINITY, 0.f};
-        for (int v = tid; v < V; v += kTreeThreads) {
-          online_add(ot, logit(trow, P.dtype, v), c);
-          online_add(od, logit(drow, P.dtype, v), c);
+        for (int o = tid; o < noct; o += kTreeThreads) {
+          float zt[8], zd[8];
+          load8(trow, P.dtype, V, o << 3, vec, zt);
+          load8(drow, P.dtype, V, o << 3, vec, zd);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            online_add(ot, zt[e], c);
+            online_add(od, zd[e], c);
+          }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -256,9 +291,15 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
           }
           // rejected: the residual's mass R_{j+1}
           float part = 0.f;
-          for (int v = tid; v < V; v += kTreeThreads) {
-            const float qv = D.q(v);
-            part += fmaxf(D.pj(v, qv) - qv, 0.f);
+          for (int o = tid; o < noct; o += kTreeThreads) {
+            float zt[8], zd[8];
+            load8(trow, P.dtype, V, o << 3, vec, zt);
+            load8(drow, P.dtype, V, o << 3, vec, zd);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float qv = D.qz(zd[e]);
+              part += fmaxf(D.pjz(zt[e], qv) - qv, 0.f);
+            }
           }
           const float R = block_sum(part, s_red);
           if (R > 0.f && D.nrej < kTreeMaxChildren) {
@@ -277,7 +318,13 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
           const int seg = (V + kTreeWarps * kTreeChunk - 1) / (kTreeWarps * kTreeChunk) * kTreeChunk;
           const int s0 = min(V, warp * seg), s1 = min(V, s0 + seg);
           float ws = 0.f;
-          for (int v = s0 + lane; v < s1; v += 32) ws += D.pj(v, D.q(v));
+          for (int v = s0 + lane * 8; v < s1; v += 256) {
+            float zt[8], zd[8];
+            load8(trow, P.dtype, s1, v, vec, zt);
+            load8(drow, P.dtype, s1, v, vec, zd);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ws += D.pjz(zt[e], D.qz(zd[e]));
+          }
           ws = warp_sum(ws);
           __syncthreads();
           if (lane == 0) s_seg[warp] = (double)ws;
@@ -300,12 +347,14 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
             const int a0 = min(V, wseg * seg), a1 = min(V, a0 + seg);
             int found = -1, lastv = -1;
             for (int cb = a0; cb < a1 && found < 0; cb += kTreeChunk) {
-              float pr[8];
+              float pr[8], zt[8], zd[8];
               float lsum = 0.f;
+              load8(trow, P.dtype, a1, cb + lane * 8, vec, zt);
+              load8(drow, P.dtype, a1, cb + lane * 8, vec, zd);
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const int v = cb + lane * 8 + e;
-                pr[e] = v < a1 ? D.pj(v, D.q(v)) : 0.f;
+                pr[e] = v < a1 ? D.pjz(zt[e], D.qz(zd[e])) : 0.f;
                 lsum += pr[e];
                 if (pr[e] > 0.f) lastv = max(lastv, v);
               }
