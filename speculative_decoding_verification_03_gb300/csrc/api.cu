@@ -218,15 +218,22 @@ sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *targe
     P.dq_tail = P.ticket + 1;
     P.dq_head = P.ticket + 2;
     P.smp = S;
-    // early exit: target rows past a sequence's first rejection are not read
-    P.lazy = 1;
-    P.ngroups = P.mode == kVerifyFull ? K + 1 : 1;
-    P.nstatic = P.nitems = P.ngroups * B * P.nch;
-    // queued target rows stay whole: measured, chunking them only adds
-    // per-chunk merge work to the chain of decisions
-    P.nch_dyn = 1;
+    // early exit: target rows past a sequence's first rejection are not
+    // read.  Used when the draft rows are streamed as well: their reads keep
+    // the GPU busy while each sequence's chain of target rows advances one
+    // decision at a time (with precomputed draft statistics the chain would
+    // run alone, and reading every verified target row at once is faster)
+    const bool early_exit = P.mode == kVerifyFull;
+    P.nch_dyn = 1;  // queued target rows stay whole (chunking them measured slower)
     P.chunk_elems_dyn = (V + kChunkAlignElems - 1) / kChunkAlignElems * kChunkAlignElems;
-    P.ndyn = B * (sp + K * P.nch_dyn);
+    if (early_exit) {
+      P.lazy = 1;
+      P.ngroups = K + 1;
+      P.nstatic = P.nitems = P.ngroups * B * P.nch;
+      P.ndyn = B * (sp + K * P.nch_dyn);
+    } else {
+      P.ndyn = B * sp;
+    }
     P.pos_cnt = reinterpret_cast<uint32_t *>(w + L.pos_cnt_off);
     clear = L.dq_off + (size_t)P.ndyn * 4;
   }
