@@ -172,3 +172,24 @@ def test_host_checks_with_gpu_present():
                      ctypes.c_void_p(out["tokens"].data_ptr()), ctypes.c_void_p(out["accept_len"].data_ptr()),
                      None, None, ctypes.c_void_p(out["ws"].data_ptr()), out["ws"].numel(), None)
     assert rc == 1  # logits not aligned to their element size
+
+
+def test_early_exit_reads_no_target_row_past_the_first_rejection():
+    """Target rows a_b + 1 .. K of every sequence (a_b from the oracle) are
+    filled with NaN: the walk must not read them (no non-finite flag) and the
+    outputs must not change."""
+    w = synth.c2(seed=9)
+    th = np.concatenate([[0.6], np.linspace(0.4, -0.4, w.K)])
+    r = oracle_verify(w, 13, theta=th)
+    g0 = gpu_verify(w, 13, theta=th)
+    poisoned = w.target.clone()
+    for b in range(w.B):
+        a = int(r["accept_len"][b])
+        if a < w.K:
+            poisoned[b, a + 1:] = float("nan")
+    w2 = synth.Workload("p", w.B, w.K, w.V, w.dtype, poisoned, w.draft, w.draft_tokens, w.temperature)
+    g = gpu_verify(w2, 13, theta=th)
+    assert g["rc"] == 0 and g["flags"] == 0, g["flags"]
+    assert np.array_equal(g["tokens"], g0["tokens"]) and np.array_equal(g["accept_len"], g0["accept_len"])
+    assert np.array_equal(g["conf"], g0["conf"])
+    assert (r["accept_len"] < w.K).sum() > w.B // 2  # most sequences had rows to skip
