@@ -231,10 +231,18 @@ sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *targe
       P.ngroups = K + 1;
       P.nstatic = P.nitems = P.ngroups * B * P.nch;
       P.ndyn = B * (sp + K * P.nch_dyn);
+      // Reading target row i + 2 one step ahead costs the rows of positions
+      // rejected at i + 1 and shortens each sequence's chain of decisions:
+      // measured faster while the streamed rows are under ~1 GB (the chains,
+      // not the bytes, bound the launch there: 64 x 5 x 32000 and
+      // 256 x 6 x 128256 bf16), slower above (1024 x 8 x 151936).
+      P.spec = (double)P.ngroups * B * V * esz < 1.0e9 ? 1 : 0;
     } else {
       P.ndyn = B * sp;
     }
     P.pos_cnt = reinterpret_cast<uint32_t *>(w + L.pos_cnt_off);
+    P.t_req = reinterpret_cast<uint32_t *>(w + L.t_req_off);
+    P.enq_cnt = reinterpret_cast<uint32_t *>(w + L.enq_cnt_off);
     clear = L.dq_off + (size_t)P.ndyn * 4;
   }
 

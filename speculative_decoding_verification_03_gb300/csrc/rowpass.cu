@@ -727,6 +727,7 @@ __device__ void lazy_finalize(const RowPassParams &P, int b, int a, int k, int l
   if (lane <= K && lane > a) P.out_tokens[(size_t)b * (K + 1) + lane] = -1;
   if (lane == 0) {
     const Part T = load_stats_cg(st + 2 * a);
+    if (a == k && (T.flags & SV_FLAG_NONFINITE)) flags |= SV_FLAG_NONFINITE;  // the bonus row
     Part D;
     D.m = 0.f;
     D.E = 0.f;
@@ -755,7 +756,9 @@ __device__ void lazy_finalize(const RowPassParams &P, int b, int a, int k, int l
     // the sample items (the task is visible first), then fillers for the
     // target rows K - a that were never queued
     __threadfence();
-    const int nfill = (K - a) * P.nch_dyn;
+    // every queued target row (including one queued ahead and not needed)
+    // counts against the sequence's K rows of queue
+    const int nfill = (K - (int)__ldcg(P.enq_cnt + b)) * P.nch_dyn;
     const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)(P.sp + nfill));
     for (int q = 0; q < P.sp; ++q) st_relaxed_gpu(P.dq + base + q, b * P.sp + q + 1);
     for (int q = 0; q < nfill; ++q) st_relaxed_gpu(P.dq + base + P.sp + q, kQueueNop);
@@ -766,70 +769,98 @@ __device__ void lazy_finalize(const RowPassParams &P, int b, int a, int k, int l
   seq_event(P, b, k, lane);
 }
 
-// Position i (< k) has both rows: test it; accept -> queue target row i + 1,
-// reject -> finalize.
-__device__ void lazy_decide(const RowPassParams &P, int b, int i, int k, int lane) {
+// Events of position i: reached (i >= 1: position i - 1 accepted), its target
+// row done, its draft row done (i < k).  The event that completes them
+// decides the position (or, at i == k, finalizes with the bonus row).
+__device__ __forceinline__ uint32_t pos_need(int i, int k) {
+  return (i >= 1 ? 1u : 0u) + 1u + (i < k ? 1u : 0u);
+}
+// lane 0: one event of position i; true when it completed the position
+__device__ __forceinline__ bool pos_event(const RowPassParams &P, int b, int i, int k) {
+  const bool done = atomicAdd(P.pos_cnt + (size_t)b * (P.K + 1) + i, 1u) == pos_need(i, k) - 1u;
+  if (done) __threadfence();
+  return done;
+}
+// lane 0: queue target row j of sequence b unless it is queued already
+__device__ __forceinline__ void queue_target(const RowPassParams &P, int b, int j) {
+  if (atomicExch(P.t_req + (size_t)b * (P.K + 1) + j, 1u) != 0u) return;
+  atomicAdd(P.enq_cnt + b, 1u);
+  const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)P.nch_dyn);
+  const int code0 = P.B * P.sp + (b * P.K + (j - 1)) * P.nch_dyn + 1;
+  for (int c = 0; c < P.nch_dyn; ++c) st_relaxed_gpu(P.dq + base + c, code0 + c);
+}
+
+// The walk from position i (all of whose events are in): test it; an
+// accepted position queues target row i + 1 and (P.spec) one step ahead row
+// i + 2, so the next link's row is often done by the time it is reached;
+// then it reaches i + 1, continuing while that position's rows are done.
+__device__ void lazy_walk(const RowPassParams &P, int b, int i, int k, int lane) {
   const int K = P.K;
-  int rej = 0;
-  if (lane == 0) {
-    const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
-    const Part T = load_stats_cg(st + 2 * i);
-    const Part D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + i) : load_stats_cg(st + 2 * i + 1);
-    const float tau_f = __ldg(P.temperature + b);
-    const bool greedy = !(tau_f > 0.f);
-    const int d = __ldg(P.draft_tokens + (size_t)b * K + i);
-    const bool in_range = d >= 0 && d < P.V;
-    const bool reject = reject_at(P, b, i, T, D, tau_f, greedy, d, in_range);
-    if (!reject) {
-      // queue target row i + 1 first: it is on the sequence's critical path
-      const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)P.nch_dyn);
-      const int code0 = P.B * P.sp + (b * K + i) * P.nch_dyn + 1;
-      for (int c = 0; c < P.nch_dyn; ++c) st_relaxed_gpu(P.dq + base + c, code0 + c);
-      P.out_tokens[(size_t)b * (K + 1) + i] = d;
+  for (;;) {
+    int rej = 0, cont = 0;
+    if (lane == 0) {
+      const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
+      const Part T = load_stats_cg(st + 2 * i);
+      const Part D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + i) : load_stats_cg(st + 2 * i + 1);
+      const float tau_f = __ldg(P.temperature + b);
+      const bool greedy = !(tau_f > 0.f);
+      const int d = __ldg(P.draft_tokens + (size_t)b * K + i);
+      const bool in_range = d >= 0 && d < P.V;
+      const bool reject = reject_at(P, b, i, T, D, tau_f, greedy, d, in_range);
+      if (T.flags & SV_FLAG_NONFINITE) atomicOr(P.status, SV_FLAG_NONFINITE);
+      if (!reject) {
+        queue_target(P, b, i + 1);                 // i + 1 <= k: on the critical path
+        if (P.spec && i + 2 <= k) queue_target(P, b, i + 2);  // speculative, one step ahead
+        P.out_tokens[(size_t)b * (K + 1) + i] = d;
+      }
+      if (P.fit) {
+        const float x = av_feature(D.E);
+        fit_label(P, i, x, av_conf(P, i, x), !reject);
+      }
+      rej = reject;
+      if (!reject) {
+        __threadfence();  // the queue count is read by whichever warp finalizes
+        cont = pos_event(P, b, i + 1, k);  // reached
+      }
     }
-    if (P.fit) {
-      const float x = av_feature(D.E);
-      fit_label(P, i, x, av_conf(P, i, x), !reject);
+    rej = __shfl_sync(0xffffffffu, rej, 0);
+    cont = __shfl_sync(0xffffffffu, cont, 0);
+    if (rej) {
+      lazy_finalize(P, b, i, k, lane);
+      return;
     }
-    rej = reject;
+    if (!cont) return;
+    ++i;
+    if (i == k) {  // every draft accepted and the bonus row is done
+      lazy_finalize(P, b, k, k, lane);
+      return;
+    }
   }
-  rej = __shfl_sync(0xffffffffu, rej, 0);
-  if (rej) lazy_finalize(P, b, i, k, lane);
 }
 
 // A row of sequence b finished (sidx = 2 i: target row i, 2 i + 1: draft row i).
 __device__ __noinline__ void lazy_row_done(const RowPassParams &P, int b, int sidx, int lane) {
   const int k = kept_len_of(P, b);
   const int i = sidx >> 1;
-  if (sidx & 1) {  // draft row i: its score, then position i may be ready
-    int ready = 0;
-    if (lane == 0) {
-      const Part D = load_stats_cg(P.stats + (size_t)b * (2 * P.K + 1) + sidx);
-      if (D.flags & SV_FLAG_NONFINITE) atomicOr(P.status, SV_FLAG_NONFINITE);
-      if (P.out_feature || P.out_conf) {
-        const float x = av_feature(D.E);
-        if (P.out_feature) P.out_feature[(size_t)b * P.K + i] = x;
-        if (P.out_conf) P.out_conf[(size_t)b * P.K + i] = av_conf(P, i, x);
-      }
-      ready = atomicAdd(P.pos_cnt + (size_t)b * (P.K + 1) + i, 1u) == 1u;
-      if (ready) __threadfence();
-    }
-    ready = __shfl_sync(0xffffffffu, ready, 0);
-    if (ready) lazy_decide(P, b, i, k, lane);
-    seq_event(P, b, k, lane);
-    return;
-  }
   int ready = 0;
   if (lane == 0) {
-    const Part T = load_stats_cg(P.stats + (size_t)b * (2 * P.K + 1) + sidx);
-    if (T.flags & SV_FLAG_NONFINITE) atomicOr(P.status, SV_FLAG_NONFINITE);
-    ready = (i == k || P.mode == kVerifyTargets) ? 1 : atomicAdd(P.pos_cnt + (size_t)b * (P.K + 1) + i, 1u) == 1u;
-    if (ready) __threadfence();
+    const Part R = load_stats_cg(P.stats + (size_t)b * (2 * P.K + 1) + sidx);
+    // a draft row is always used (its AV score); a target row's flags are
+    // raised when its position is decided (it may have been read ahead)
+    if ((sidx & 1) && (R.flags & SV_FLAG_NONFINITE)) atomicOr(P.status, SV_FLAG_NONFINITE);
+    if ((sidx & 1) && (P.out_feature || P.out_conf)) {  // a draft row's score
+      const float x = av_feature(R.E);
+      if (P.out_feature) P.out_feature[(size_t)b * P.K + i] = x;
+      if (P.out_conf) P.out_conf[(size_t)b * P.K + i] = av_conf(P, i, x);
+    }
+    ready = pos_event(P, b, i, k);
   }
   ready = __shfl_sync(0xffffffffu, ready, 0);
-  if (!ready) return;
-  if (i == k) lazy_finalize(P, b, k, k, lane);  // every draft accepted: bonus from row k
-  else lazy_decide(P, b, i, k, lane);
+  if (ready) {
+    if (i == k) lazy_finalize(P, b, k, k, lane);  // every draft accepted: bonus from row k
+    else lazy_walk(P, b, i, k, lane);
+  }
+  if (sidx & 1) seq_event(P, b, k, lane);
 }
 
 __device__ void finish_score(const RowPassParams &P, int b, int lane) {

@@ -174,10 +174,11 @@ def test_host_checks_with_gpu_present():
     assert rc == 1  # logits not aligned to their element size
 
 
-def test_early_exit_reads_no_target_row_past_the_first_rejection():
+def test_early_exit_uses_no_target_row_past_the_first_rejection():
     """Target rows a_b + 1 .. K of every sequence (a_b from the oracle) are
-    filled with NaN: the walk must not read them (no non-finite flag) and the
-    outputs must not change."""
+    filled with NaN: the walk must not use them (no non-finite flag) and the
+    outputs must not change.  (Row a_b + 1 may be read one step ahead on
+    small launches, and is then discarded.)"""
     w = synth.c2(seed=9)
     th = np.concatenate([[0.6], np.linspace(0.4, -0.4, w.K)])
     r = oracle_verify(w, 13, theta=th)
