@@ -38,6 +38,68 @@ __device__ __forceinline__ float key_survival(uint64_t key) {
   return __uint_as_float(0xffffffffu - (uint32_t)(key >> 32));
 }
 
+// Bitonic sort of npad = 1024 E keys in shared memory (ascending), E keys
+// per thread in registers (thread t holds keys t E .. t E + E - 1).
+template <int E>
+__device__ void bitonic_sort(uint64_t *keys, int npad) {
+  const int tid = threadIdx.x;
+  uint64_t r[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) r[e] = keys[tid * E + e];
+  for (int size = 2; size <= npad; size <<= 1) {
+    int stride = size >> 1;
+    if (stride >= 32 * E) {  // partners in other warps: through shared memory
+#pragma unroll
+      for (int e = 0; e < E; ++e) keys[tid * E + e] = r[e];
+      __syncthreads();
+      for (; stride >= 32 * E; stride >>= 1) {
+        const int sh = __ffs(stride) - 1;
+        for (int q = tid; q < (npad >> 1); q += kBudgetThreads) {
+          const int lo = ((q >> sh) << (sh + 1)) + (q & (stride - 1)), hi = lo + stride;
+          const bool up = (lo & size) == 0;
+          const uint64_t x = keys[lo], y = keys[hi];
+          if ((x > y) == up) {
+            keys[lo] = y;
+            keys[hi] = x;
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) r[e] = keys[tid * E + e];
+    }
+    for (; stride >= E; stride >>= 1) {  // partners in the same warp: shuffles
+      const int lm = stride / E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, r[e], lm);
+        const int i = tid * E + e;
+        const bool keep_min = ((i & stride) == 0) == ((i & size) == 0);
+        r[e] = keep_min ? (o < r[e] ? o : r[e]) : (o > r[e] ? o : r[e]);
+      }
+    }
+#pragma unroll
+    for (int st = E / 2; st >= 1; st >>= 1) {  // partners in the same thread
+      if (st <= stride) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          if (e & st) continue;
+          const bool up = ((tid * E + e) & size) == 0;
+          if ((r[e] > r[e + st]) == up) {
+            const uint64_t t = r[e];
+            r[e] = r[e + st];
+            r[e + st] = t;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();  // every thread is done reading keys before they are rewritten
+#pragma unroll
+  for (int e = 0; e < E; ++e) keys[tid * E + e] = r[e];
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const BudgetParams P) {
   extern __shared__ uint64_t keys[];
   __shared__ float s_whi[kBudgetWarps], s_wlo[kBudgetWarps], s_bf[kBudgetWarps];
@@ -66,21 +128,14 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const Budg
   for (int j = NK + tid; j < npad; j += kBudgetThreads) keys[j] = ~0ull;
   __syncthreads();
 
-  // 2. bitonic sort, ascending keys (strides are powers of two: shifts)
-  for (int size = 2; size <= npad; size <<= 1) {
-    for (int sh = __ffs(size) - 2; sh >= 0; --sh) {
-      const int stride = 1 << sh;
-      for (int t = tid; t < (npad >> 1); t += kBudgetThreads) {
-        const int lo = ((t >> sh) << (sh + 1)) + (t & (stride - 1)), hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const uint64_t x = keys[lo], y = keys[hi];
-        if ((x > y) == up) {
-          keys[lo] = y;
-          keys[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
+  // 2. bitonic sort, ascending keys: each thread holds npad / 1024 keys in
+  //    registers; strides below that stay in registers, strides up to 32x
+  //    that go through warp shuffles, larger ones through shared memory
+  switch (npad >> 10) {
+    case 2: bitonic_sort<2>(keys, npad); break;
+    case 4: bitonic_sort<4>(keys, npad); break;
+    case 8: bitonic_sort<8>(keys, npad); break;
+    default: bitonic_sort<16>(keys, npad); break;
   }
 
   // 3. number of candidates: the first non-candidate key
@@ -210,7 +265,7 @@ extern "C" sv_status_t sv_av_budget(int B, int K, const float *conf, const int32
   int sms = 0;
   const sv_status_t ds = host_device_info(&sms);
   if (ds != SV_OK) return ds;
-  int npad = 2;
+  int npad = 2048;  // at least two keys per thread of the sort
   while (npad < B * K) npad <<= 1;
   const size_t smem = (size_t)npad * sizeof(uint64_t) + (size_t)B * K * sizeof(float);
   const cudaError_t e = cudaFuncSetAttribute(av_budget_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
