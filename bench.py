@@ -54,7 +54,7 @@ def _peak():
 def _kernel_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_03_gb300", "csrc")
-    for fn in ("rowpass.cu", "sv_device.cuh", "sv_internal.h", "sample_common.cuh", "avfit_common.cuh"):
+    for fn in ("rowpass.cu", "api.cu", "sv_device.cuh", "sv_internal.h", "sample_common.cuh", "avfit_common.cuh"):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -151,16 +151,19 @@ def _aggregate(elapsed_ms: float, units: float, device):
 
 
 def _bytes_per_step(wl, K, V, esz, kept, accept):
-    """Algorithmic bytes of one step.  Returns (bytes of the verify row-pass
-    launch that the launch events bracket, all bytes of the step).  The
-    acceptance walk needs target rows 0 .. a_b only (the row after the last
-    accepted draft; nothing past the first rejection is read) and every
-    verified draft row (k_b of them: they carry the AV scores); the second
-    pass re-reads the residual or bonus target row (+ the draft row when
-    rejected); 4 B (3K + 4) of small per-sequence inputs and outputs.  On the
-    AV-truncated canvas the scoring call reads all K draft rows and the verify
-    row pass only target rows (plus the second pass).  The eager count (every
-    verified target row k_b + 1) is returned as well, for comparison."""
+    """Bytes of one step.  Returns (early-exit bytes of the verify row-pass
+    launch that the launch events bracket, early-exit bytes of the whole
+    step, algorithmic bytes of the bracketed launch).
+
+    Algorithmic bytes (the roofline's numerator): every verified target row
+    (k_b + 1 per sequence) and every verified draft row (k_b; on the
+    AV-truncated canvas the scoring launch reads the draft rows instead), the
+    residual or bonus target row once more (+ the draft row when rejected),
+    and 4 B (3K + 4) of small per-sequence inputs and outputs.
+
+    Early-exit bytes: what the acceptance walk cannot avoid -- target rows
+    0 .. a_b only (nothing past the first rejection is read) -- plus the same
+    draft rows, second pass and small arrays."""
     B = kept.size
     second = int(B + (accept < kept).sum()) * V * esz
     small = 4 * B * (3 * K + 4)
@@ -281,17 +284,21 @@ def run_gpu(args):
     # on the AV-truncated canvas both row passes of a step record the same
     # event pair; the later (verify) launch is the one that stays bracketed
     rp_ms = sum(rowpass_ms) / len(rowpass_ms)
-    rp_bytes = bytes_rp / args.steps
+    # algorithmic bytes: every verified row once, the residual or bonus row
+    # again, the small per-sequence arrays -- a fixed definition that does
+    # not depend on how much of it the kernel gets to skip
+    rp_bytes = bytes_eager / args.steps
     achieved = rp_bytes / (rp_ms / 1e3) / 1e9
+    ee_bytes = bytes_rp / args.steps
     res["roofline"] = dict(bound="hbm", kernel="rowpass_kernel", achieved=achieved, peak=peak, unit="GB/s",
                            frac=achieved / peak, peak_source="%s (MEASURED_PEAKS hbm_gbs)" % peak_kind
                            if peak_kind == "measured" else "fallback 6.8 TB/s",
                            traffic=_traffic(args.workload), algorithmic_bytes_per_launch=rp_bytes,
                            ms_per_launch=rp_ms,
-                           # the same launch counted with every verified target row read
-                           # (the definition without early exit), for comparison
-                           eager_bytes_per_launch=bytes_eager / args.steps,
-                           frac_eager_bytes=bytes_eager / args.steps / (rp_ms / 1e3) / 1e9 / peak)
+                           # the bytes the early-exit walk actually needs (no target
+                           # row past the first rejection), and the bandwidth on them
+                           early_exit_bytes_per_launch=ee_bytes,
+                           frac_early_exit_bytes=ee_bytes / (rp_ms / 1e3) / 1e9 / peak)
     res["step_hbm"] = dict(algorithmic_bytes_per_step=bytes_all / args.steps,
                            achieved_gbs=bytes_all / args.steps / (elapsed_ms / args.steps / 1e3) / 1e9)
     res["gpu_launches"] = launches_per_step * args.steps
