@@ -18,7 +18,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = ["api.cu", "rowpass.cu", "sample.cu", "avfit.cu", "postverify.cu", "budget.cu", "tts.cu", "tree.cu"]
+_SOURCES = ["api.cu", "rowpass.cu", "walk.cu", "sample.cu", "avfit.cu", "postverify.cu", "budget.cu", "tts.cu", "tree.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC"]
 
@@ -40,7 +40,7 @@ def build(force: bool = False, nvcc: str = "nvcc") -> str:
     """Compile the CUDA sources for sm_103a into libspecverify.so (in-tree)."""
     csrc = os.path.join(_HERE, "csrc")
     srcs = [os.path.join(csrc, s) for s in _SOURCES]
-    deps = srcs + [os.path.join(csrc, h) for h in ("sv_device.cuh", "sv_internal.h", "sample_common.cuh",
+    deps = srcs + [os.path.join(csrc, h) for h in ("sv_device.cuh", "sv_internal.h", "sample_common.cuh", "rowstats.cuh",
                                                    "avfit_common.cuh")] + \
         [os.path.join(_ROOT, "include", "specverify.h")]
     if not force and os.path.exists(LIB_PATH) and \
