@@ -18,7 +18,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _ROOT = os.path.dirname(_HERE)
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = ["api.cu", "rowpass.cu", "walk.cu", "sample.cu", "avfit.cu", "postverify.cu", "budget.cu", "tts.cu", "tree.cu"]
+_SOURCES = ["api.cu", "rowpass.cu", "sample.cu", "avfit.cu", "postverify.cu", "budget.cu", "tts.cu", "tree.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC"]
 

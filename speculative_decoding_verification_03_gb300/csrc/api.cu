@@ -13,10 +13,6 @@ cudaError_t launch_rowpass(const RowPassParams &P, int grid, cudaStream_t stream
 cudaError_t launch_sample(const SampleParams &P, int grid, cudaStream_t stream);
 cudaError_t launch_avfit(const FitParams &P, int grid, cudaStream_t stream);
 cudaError_t launch_philox(uint64_t seed, int nb, int npos, uint32_t *out, cudaStream_t stream);
-size_t walk_smem_head();
-const void *walk_kernel_fn(int dtype);
-int walk_threads();
-cudaError_t launch_walk(const WalkParams &W, size_t smem, cudaStream_t stream);
 }  // namespace sv
 
 using namespace sv;
@@ -110,105 +106,6 @@ cudaError_t rowpass_timed(const RowPassParams &P, int grid, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (t_ev_end) e = cudaEventRecord(t_ev_end, st);
   return e;
-}
-
-cudaError_t walk_timed(const WalkParams &W, size_t smem, cudaStream_t st) {
-  cudaError_t e = cudaSuccess;
-  if (t_ev_begin && (e = cudaEventRecord(t_ev_begin, st)) != cudaSuccess) return e;
-  e = launch_walk(W, smem, st);
-  if (e != cudaSuccess) return e;
-  if (t_ev_end) e = cudaEventRecord(t_ev_end, st);
-  return e;
-}
-
-// Cluster walk configuration for one (V, element size): the smallest cluster
-// whose slices (a multiple of 256 elements, at most one 48 KB copy) leave room
-// for a ring of at least 6 slots, else the smallest with at least 4.
-struct WalkCfg {
-  int cs, slice, slot_bytes, nslot, clusters;
-  size_t smem;
-};
-
-bool walk_cfg_uncached(int V, int esz, int dtype, WalkCfg *out) {
-  int dev = 0, optin = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
-  const size_t head = walk_smem_head();
-  const void *fn = walk_kernel_fn(dtype);
-  WalkCfg pick{0, 0, 0, 0, 0, 0};
-  for (int cs : {1, 2, 4, 8}) {
-    const int slice = ((V + cs - 1) / cs + kSubChunk - 1) / kSubChunk * kSubChunk;
-    if ((size_t)slice * esz > (size_t)kStageBytes) continue;
-    const int slot_bytes = (int)align_up((size_t)slice * esz, 128);
-    if ((size_t)optin < head + 4 * (size_t)slot_bytes) continue;
-    int nslot = (int)(((size_t)optin - head) / (size_t)slot_bytes);
-    if (nslot > kWalkMaxSlots) nslot = kWalkMaxSlots;
-    const size_t smem = head + (size_t)nslot * slot_bytes;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
-      cudaGetLastError();
-      continue;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs, 1, 1);
-    cfg.blockDim = dim3(walk_threads(), 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = cs;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int ncl = 0;
-    if (cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg) != cudaSuccess || ncl < 1) {
-      cudaGetLastError();
-      continue;
-    }
-    const WalkCfg c{cs, slice, slot_bytes, nslot, ncl, smem};
-    if (!pick.cs) pick = c;
-    if (nslot >= 6) {
-      pick = c;
-      break;
-    }
-  }
-  if (!pick.cs) return false;
-  // the attribute must hold the chosen size (the loop may have set another)
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pick.smem) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  *out = pick;
-  return true;
-}
-
-std::mutex g_walk_mu;
-struct WalkCacheEnt {
-  int dev, V, dtype, ok;
-  WalkCfg cfg;
-};
-WalkCacheEnt g_walk_cache[16];
-int g_walk_n = 0;
-
-bool walk_cfg(int V, int esz, int dtype, WalkCfg *out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  std::lock_guard<std::mutex> lk(g_walk_mu);
-  for (int i = 0; i < g_walk_n; ++i)
-    if (g_walk_cache[i].dev == dev && g_walk_cache[i].V == V && g_walk_cache[i].dtype == dtype) {
-      if (!g_walk_cache[i].ok) return false;
-      // another size for the same kernel may have been configured since
-      if (cudaFuncSetAttribute(walk_kernel_fn(dtype), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)g_walk_cache[i].cfg.smem) != cudaSuccess)
-        return false;
-      *out = g_walk_cache[i].cfg;
-      return true;
-    }
-  WalkCfg cfg{};
-  const bool ok = walk_cfg_uncached(V, esz, dtype, &cfg);
-  WalkCacheEnt &e = g_walk_cache[g_walk_n < 16 ? g_walk_n++ : 15];
-  e = WalkCacheEnt{dev, V, dtype, ok ? 1 : 0, cfg};
-  *out = cfg;
-  return ok;
 }
 
 }  // namespace
@@ -347,39 +244,6 @@ sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *targe
     P.t_req = reinterpret_cast<uint32_t *>(w + L.t_req_off);
     P.enq_cnt = reinterpret_cast<uint32_t *>(w + L.enq_cnt_off);
     clear = L.dq_off + (size_t)P.ndyn * 4;
-  }
-
-  // The fused step with streamed draft rows can walk each sequence inside one
-  // thread-block cluster when the rows are 16-byte aligned and a row's
-  // slices fit the clusters' shared memory (walk.cu); the streaming row pass
-  // below handles every other case.
-  // Measured: the walk is faster while each cluster walks at most two
-  // sequences (64 x 5 x 32000 bf16: 64 us against 80 us); larger batches
-  // stream (256 x 6 x 128256: 400 us against 160 us).
-  WalkCfg wc;
-  if (P.fused && P.mode == kVerifyFull && walk_cfg(V, esz, (int)dtype, &wc) && B <= 2 * wc.clusters) {
-    WalkParams W{};
-    std::memset(&W, 0, sizeof W);
-    W.R = P;
-    W.cs = wc.cs;
-    W.slice = wc.slice;
-    W.slot_bytes = wc.slot_bytes;
-    W.nslot = wc.nslot;
-    W.window = wc.nslot + 1;
-    W.nclusters = wc.clusters < B ? wc.clusters : B;
-    W.seq_ticket = P.ticket;
-    // the give-up record goes to the row-statistics area (unused on this path)
-    const size_t cap = (L.chunk_off - L.stats_off) / sizeof(int);
-    W.giveup = reinterpret_cast<int *>(w + L.stats_off);
-    W.giveup_cap = cap > (size_t)(1 << 20) ? (1 << 20) : (int)cap;
-    // status word, tickets, completion count and refit sums; the give-up record
-    cudaError_t e = cudaMemsetAsync(w, 0, L.fitacc_off + (size_t)SV_MAX_K * kFitQ * 8, st);
-    if (e != cudaSuccess) return SV_ERR_CUDA;
-    const int rec = 96 + 4 * W.nclusters * W.cs;
-    if (W.giveup_cap >= rec) e = cudaMemsetAsync(W.giveup, 0, (size_t)rec * sizeof(int), st);
-    else W.giveup_cap = 0;
-    if (e != cudaSuccess) return SV_ERR_CUDA;
-    return cuda_status(walk_timed(W, wc.smem, st));
   }
 
   // status word (offset 0) and the per-call counters, in one clear

@@ -1,5 +1,5 @@
-// Row statistics and per-position decisions shared by the streaming row pass
-// (rowpass.cu) and the cluster walk (walk.cu).
+// Row statistics and per-position decisions of the streaming row pass
+// (rowpass.cu).
 //
 // Per vocabulary row ("Speculative Decoding: Draft, EAGLE, MTP", section "one
 // speculative step"): the raw maximum m, the first argmax, and

@@ -205,86 +205,6 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
   return v;
 }
 
-// Cluster-scope mbarrier use: a wait that acquires what other CTAs of the
-// cluster released, an arrive on a barrier in another CTA, and a 16-byte
-// store into another CTA's shared memory.
-__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_try_wait_cl_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-// non-blocking test of a phase (cluster-scope acquire), for polling loops
-__device__ __forceinline__ bool mbar_test_wait_cl(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// 16-byte store into another CTA's shared memory that completes 16 bytes of
-// transaction count on an mbarrier in that CTA (both shared::cluster
-// addresses of the same CTA): the receiver's ordinary wait on the barrier
-// then sees the data, with no cluster-scope fence on either side.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t mbar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                   addr),
-               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar)
-               : "memory");
-}
-// non-blocking test of a local phase
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// CTA-scope release store / acquire load of a shared-memory word (a counter
-// one warp publishes and another polls)
-__device__ __forceinline__ void st_release_cta_shared(int* p, int v) {
-  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire_cta_shared(const int* p) {
-  int v;
-  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
-  return v;
-}
-// arrive (release, cluster scope) on the barrier at shared::cluster address
-// `addr` (from mapa_shared)
-__device__ __forceinline__ void mbar_arrive_cl(uint32_t addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Numerics.
 // ---------------------------------------------------------------------------

@@ -138,32 +138,6 @@ struct RowPassParams {
 };
 
 
-// ---- cluster walk (walk.cu) ----------------------------------------------------
-// The fused verification step (target and draft rows streamed, no supplied
-// draft statistics) with each sequence walked inside one thread-block
-// cluster: every row is split into `cs` slices of `slice` elements, one per
-// CTA, so that the row a decision waits for arrives in a fraction of the time
-// one SM would take to stream it.
-constexpr int kWalkSeqs = 6;       // sequences a cluster walks at once
-constexpr int kWalkMaxSlots = 8;   // TMA ring slots per CTA
-constexpr int kWalkMaxCs = 8;      // CTAs per cluster
-
-struct WalkParams {
-  RowPassParams R;   // rows, outputs, refit and workspace pointers
-  int cs;            // CTAs per cluster (1, 2, 4 or 8)
-  int slice;         // elements per CTA slice: a multiple of kSubChunk, slice * esz <= kStageBytes
-  int slot_bytes;    // ring slot stride (slice * esz rounded up to 128)
-  int nslot;         // ring slots per CTA
-  int window;        // row entries a cluster keeps in flight
-  int nclusters;     // clusters launched
-  uint32_t *seq_ticket;  // sequences taken after the first kWalkSeqs * nclusters
-  // where a launch gave up (written only after a time-out): [0] claimed by the
-  // first cluster to record, [1 .. 95] its leader's state, then per CTA and
-  // role (math, producer, epilogue, leader) the entry it stopped at + 1
-  int *giveup;
-  int giveup_cap;    // ints available at giveup (0: no record)
-};
-
 // ---- workspace layout --------------------------------------------------------
 constexpr int kMaxSampleParts = 16;
 
