@@ -16,6 +16,7 @@
 // target argmax.
 #include <cfloat>
 
+#include "sample_common.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -26,6 +27,7 @@ constexpr int kTreeThreads = 512;
 constexpr int kTreeWarps = kTreeThreads / 32;
 constexpr int kTreeChunk = 256;  // tokens per lane-pass of the final draw (8 per lane)
 constexpr int kTreeMaxChildren = SV_TREE_MAX_NODES - 1;
+constexpr int kTreeMaxChunkSums = 32;  // 256-token chunk sums a warp keeps for the staged draw
 
 struct TreeParams {
   int B, N, V, dtype;
@@ -37,29 +39,42 @@ struct TreeParams {
   uint32_t *out_flags;
 };
 
+// Row reads: from global memory (L2, .cg) or, when the node's rows were
+// staged (kS), from shared memory through generic addresses.
+template <bool kS>
+__device__ __forceinline__ uint4 ld16(const uint4 *p) {
+  if (kS) return *p;
+  return __ldcg(p);
+}
+template <bool kS>
 __device__ __forceinline__ float logit(const void *row, int dtype, int v) {
-  if (dtype == SV_BF16) return __uint_as_float(((uint32_t)__ldcg(reinterpret_cast<const unsigned short *>(row) + v)) << 16);
-  return __ldcg(reinterpret_cast<const float *>(row) + v);
+  if (dtype == SV_BF16) {
+    const unsigned short *r = reinterpret_cast<const unsigned short *>(row) + v;
+    return __uint_as_float(((uint32_t)(kS ? *r : __ldcg(r))) << 16);
+  }
+  const float *r = reinterpret_cast<const float *>(row) + v;
+  return kS ? *r : __ldcg(r);
 }
 
 // Eight consecutive logits v .. v+7 (v a multiple of 8) of a row: one or two
 // 16-byte loads when the row is 16-byte aligned, else plain loads; tokens at
 // or beyond V read as -inf.
+template <bool kS>
 __device__ __forceinline__ void load8(const void *row, int dtype, int V, int v, bool vec, float (&z)[8]) {
   if (vec && v + 8 <= V) {
     if (dtype == SV_BF16) {
-      const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(row) + (v >> 3));
+      const uint4 w = ld16<kS>(reinterpret_cast<const uint4 *>(row) + (v >> 3));
       z[0] = bf16lo(w.x); z[1] = bf16hi(w.x); z[2] = bf16lo(w.y); z[3] = bf16hi(w.y);
       z[4] = bf16lo(w.z); z[5] = bf16hi(w.z); z[6] = bf16lo(w.w); z[7] = bf16hi(w.w);
     } else {
-      const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(row) + (v >> 2));
-      const uint4 b = __ldcg(reinterpret_cast<const uint4 *>(row) + (v >> 2) + 1);
+      const uint4 a = ld16<kS>(reinterpret_cast<const uint4 *>(row) + (v >> 2));
+      const uint4 b = ld16<kS>(reinterpret_cast<const uint4 *>(row) + (v >> 2) + 1);
       z[0] = __uint_as_float(a.x); z[1] = __uint_as_float(a.y); z[2] = __uint_as_float(a.z); z[3] = __uint_as_float(a.w);
       z[4] = __uint_as_float(b.x); z[5] = __uint_as_float(b.y); z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) z[e] = v + e < V ? logit(row, dtype, v + e) : -INFINITY;
+    for (int e = 0; e < 8; ++e) z[e] = v + e < V ? logit<kS>(row, dtype, v + e) : -INFINITY;
   }
 }
 
@@ -85,25 +100,24 @@ __device__ __forceinline__ Online online_merge(Online a, Online b, float c) {
   return a;
 }
 
+template <bool kS>
 struct NodeDist {
   float c, Mt, Md, inv_St, inv_Sd;
   const void *trow, *drow;
   int dtype;
-  // residual chain: p_0 = p; p_{j+1} = max(p_j - q, 0) * invR[j]
-  int nrej;
-  float invR[kTreeMaxChildren];
+  // residual chain p_0 = p, p_{j+1} = max(p_j - q, 0) / R_{j+1}, in closed
+  // form: p_j = max(p_0 - a_j q, 0) / Z_j with a_0 = 0, Z_0 = 1,
+  // a_{j+1} = a_j + Z_j, Z_{j+1} = Z_j R_{j+1} (by induction: where
+  // p_0 <= a_j q both sides are 0; elsewhere p_j - q = (p_0 - (a_j + Z_j) q) / Z_j)
+  float a, invZ;
   __device__ __forceinline__ float p0z(float zt) const { return ex2_approx((zt - Mt) * c) * inv_St; }
   __device__ __forceinline__ float qz(float zd) const { return ex2_approx((zd - Md) * c) * inv_Sd; }
-  __device__ __forceinline__ float p0(int v) const { return p0z(logit(trow, dtype, v)); }
-  __device__ __forceinline__ float q(int v) const { return qz(logit(drow, dtype, v)); }
+  __device__ __forceinline__ float p0(int v) const { return p0z(logit<kS>(trow, dtype, v)); }
+  __device__ __forceinline__ float q(int v) const { return qz(logit<kS>(drow, dtype, v)); }
   // p_j(v) for j = nrej (the current residual) and the un-normalised
   // max(p_j - q, 0) for the next step
-  __device__ __forceinline__ float pj(int v, float qv) const { return pjz(logit(trow, dtype, v), qv); }
-  __device__ __forceinline__ float pjz(float zt, float qv) const {
-    float r = p0z(zt);
-    for (int i = 0; i < nrej; ++i) r = fmaxf(r - qv, 0.f) * invR[i];
-    return r;
-  }
+  __device__ __forceinline__ float pj(int v, float qv) const { return pjz(logit<kS>(trow, dtype, v), qv); }
+  __device__ __forceinline__ float pjz(float zt, float qv) const { return fmaxf(fmaf(-a, qv, p0z(zt)), 0.f) * invZ; }
 };
 
 __device__ __forceinline__ float block_sum(float v, float *scratch) {
@@ -117,8 +131,16 @@ __device__ __forceinline__ float block_sum(float v, float *scratch) {
   return s;
 }
 
+template <bool kS>
 __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams P) {
+  extern __shared__ __align__(128) uint8_t tree_smem[];
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ int s_abort;
+  __shared__ uint32_t s_status;
+  uint32_t bar_phase = 0;
   __shared__ int s_kids[kTreeMaxChildren + 1];
+  __shared__ int s_par[SV_TREE_MAX_NODES], s_tokn[SV_TREE_MAX_NODES];
+  __shared__ float s_csum[kS ? kTreeWarps * kTreeMaxChunkSums : 1];
   __shared__ int s_nkids;
   __shared__ float s_red[kTreeWarps];
   __shared__ Online s_on_t[kTreeWarps], s_on_d[kTreeWarps];
@@ -129,6 +151,18 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = P.N, V = P.V;
   const int esz = P.dtype == SV_BF16 ? 2 : 4;
+  const uint32_t row_bytes = (uint32_t)P.V * (uint32_t)esz;
+  uint8_t *s_trow = tree_smem;
+  uint8_t *s_drow = tree_smem + ((row_bytes + 127u) & ~127u);
+  if (kS) {
+    if (tid == 0) {
+      mbar_init(&s_bar, 1);
+      s_abort = 0;
+      s_status = 0u;
+      fence_barrier_init();
+    }
+    __syncthreads();
+  }
   for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
     const int32_t *par = P.parents + (size_t)b * N;
     const int32_t *tok = P.tokens + (size_t)b * N;
@@ -138,9 +172,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
     if (tid == 0) s_bad = (nb < 1 || nb > N) ? 1 : 0;
     __syncthreads();
     if (!s_bad)
-      for (int n = 1 + tid; n < nb; n += kTreeThreads) {
+      for (int n = tid; n < nb; n += kTreeThreads) {
         const int pn = __ldg(par + n);
-        if (pn < 0 || pn >= n) s_bad = 1;
+        s_par[n] = pn;
+        s_tokn[n] = __ldg(tok + n);
+        if (n >= 1 && (pn < 0 || pn >= n)) s_bad = 1;
       }
     for (int j = tid; j < N; j += kTreeThreads) out[j] = -1;
     if (path)
@@ -165,7 +201,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         int cnt = 0;
         for (int base = 1; base < nb; base += 32) {
           const int n = base + lane;
-          const bool is_kid = n < nb && __ldg(par + n) == cur;
+          const bool is_kid = n < nb && s_par[n] == cur;
           const unsigned m = __ballot_sync(0xffffffffu, is_kid);
           if (is_kid) {
             const int slot = cnt + __popc(m & ((1u << lane) - 1u));
@@ -179,7 +215,33 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       const int nk = s_nkids;
       const void *trow = reinterpret_cast<const char *>(P.target) + ((size_t)b * N + cur) * (size_t)V * esz;
       const void *drow = reinterpret_cast<const char *>(P.draft) + ((size_t)b * N + cur) * (size_t)V * esz;
-      const bool vec = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(drow)) & 15) == 0;
+      bool vec = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(drow)) & 15) == 0;
+      if (kS) {
+        // node cur's rows into shared memory (one bulk copy each; the draft
+        // row only for sampled rows), then every pass reads them there
+        if (tid == 0) {
+          // the previous node's reads (generic proxy) before the copies overwrite them
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          const uint32_t bytes = greedy ? row_bytes : 2u * row_bytes;
+          mbar_arrive_expect_tx(&s_bar, bytes);
+          bulk_g2s(s_trow, trow, row_bytes, &s_bar);
+          if (!greedy) bulk_g2s(s_drow, drow, row_bytes, &s_bar);
+        }
+        // bounded (2 s): a copy that never lands flags the request and stops
+        // the CTA (nothing else in flight)
+        const bool got = mbar_wait_bounded(&s_bar, bar_phase, &s_abort, &s_status, 2000000000ull);
+        if (!__syncthreads_and(got)) {
+          if (tid == 0) {
+            P.out_accept_len[b] = 0;
+            if (P.out_flags) P.out_flags[b] = SV_TREE_BAD;
+          }
+          return;
+        }
+        bar_phase ^= 1u;
+        trow = s_trow;
+        drow = s_drow;
+        vec = true;
+      }
       const int noct = (V + 7) >> 3;  // groups of 8 consecutive tokens
       int next = -1;
       if (greedy) {
@@ -188,7 +250,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         int bi = INT_MAX;
         for (int o = tid; o < noct; o += kTreeThreads) {
           float z[8];
-          load8(trow, P.dtype, V, o << 3, vec, z);
+          load8<kS>(trow, P.dtype, V, o << 3, vec, z);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             if (z[e] > bv) {
@@ -223,7 +285,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         __syncthreads();
         const int best = s_tok;
         for (int j = 0; j < nk; ++j)
-          if (__ldg(tok + s_kids[j]) == best) {
+          if (s_tokn[s_kids[j]] == best) {
             next = s_kids[j];
             break;
           }
@@ -234,10 +296,64 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
       } else {
         // statistics of both rows
         Online ot = {-INFINITY, 0.f}, od = {-INFINITY, 0.f};
+        if (kS) {
+          // rows in shared memory: the maxima first, then the sums
+          float mt = -INFINITY, md = -INFINITY;
+          for (int o = tid; o < noct; o += kTreeThreads) {
+            float zt[8], zd[8];
+            load8<kS>(trow, P.dtype, V, o << 3, vec, zt);
+            load8<kS>(drow, P.dtype, V, o << 3, vec, zd);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              mt = fmaxf(mt, zt[e]);
+              md = fmaxf(md, zd[e]);
+            }
+          }
+          mt = warp_max(mt);
+          md = warp_max(md);
+          if (lane == 0) {
+            s_on_t[warp].m = mt;
+            s_on_d[warp].m = md;
+          }
+          __syncthreads();
+          mt = s_on_t[0].m;
+          md = s_on_d[0].m;
+          for (int i = 1; i < kTreeWarps; ++i) {
+            mt = fmaxf(mt, s_on_t[i].m);
+            md = fmaxf(md, s_on_d[i].m);
+          }
+          float st = 0.f, sd = 0.f;
+          for (int o = tid; o < noct; o += kTreeThreads) {
+            float zt[8], zd[8];
+            load8<kS>(trow, P.dtype, V, o << 3, vec, zt);
+            load8<kS>(drow, P.dtype, V, o << 3, vec, zd);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              if (mt > -INFINITY) st += ex2_approx((zt[e] - mt) * c);
+              if (md > -INFINITY) sd += ex2_approx((zd[e] - md) * c);
+            }
+          }
+          st = warp_sum(st);
+          sd = warp_sum(sd);
+          __syncthreads();  // the maxima are read
+          if (lane == 0) {
+            s_on_t[warp].s = st;
+            s_on_d[warp].s = sd;
+          }
+          __syncthreads();
+          st = 0.f;
+          sd = 0.f;
+          for (int i = 0; i < kTreeWarps; ++i) {
+            st += s_on_t[i].s;
+            sd += s_on_d[i].s;
+          }
+          ot = {mt, st};
+          od = {md, sd};
+        } else {
         for (int o = tid; o < noct; o += kTreeThreads) {
           float zt[8], zd[8];
-          load8(trow, P.dtype, V, o << 3, vec, zt);
-          load8(drow, P.dtype, V, o << 3, vec, zd);
+          load8<kS>(trow, P.dtype, V, o << 3, vec, zt);
+          load8<kS>(drow, P.dtype, V, o << 3, vec, zd);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             online_add(ot, zt[e], c);
@@ -262,7 +378,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
           ot = online_merge(ot, s_on_t[i], c);
           od = online_merge(od, s_on_d[i], c);
         }
-        NodeDist D;
+        }
+        NodeDist<kS> D;
         D.c = c;
         D.Mt = ot.m;
         D.Md = od.m;
@@ -271,10 +388,11 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         D.trow = trow;
         D.drow = drow;
         D.dtype = P.dtype;
-        D.nrej = 0;
+        D.a = 0.f;
+        D.invZ = 1.f;
         for (int j = 0; j < nk; ++j) {
           const int child = s_kids[j];
-          const int x = __ldg(tok + child);
+          const int x = s_tokn[child];
           // acceptance test of child j (every thread computes it identically)
           float ratio = 0.f;
           if (x >= 0 && x < V) {
@@ -293,8 +411,8 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
           float part = 0.f;
           for (int o = tid; o < noct; o += kTreeThreads) {
             float zt[8], zd[8];
-            load8(trow, P.dtype, V, o << 3, vec, zt);
-            load8(drow, P.dtype, V, o << 3, vec, zd);
+            load8<kS>(trow, P.dtype, V, o << 3, vec, zt);
+            load8<kS>(drow, P.dtype, V, o << 3, vec, zd);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float qv = D.qz(zd[e]);
@@ -302,9 +420,9 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
             }
           }
           const float R = block_sum(part, s_red);
-          if (R > 0.f && D.nrej < kTreeMaxChildren) {
-            D.invR[D.nrej] = 1.f / R;
-            ++D.nrej;
+          if (R > 0.f) {
+            D.a += 1.f / D.invZ;
+            D.invZ /= R;
           } else {
             flags |= SV_TREE_ZERO_RESIDUAL;
           }
@@ -317,68 +435,153 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
           const float u = (float)(r.w[1] >> 8) * (1.0f / 16777216.0f);
           const int seg = (V + kTreeWarps * kTreeChunk - 1) / (kTreeWarps * kTreeChunk) * kTreeChunk;
           const int s0 = min(V, warp * seg), s1 = min(V, s0 + seg);
-          float ws = 0.f;
-          for (int v = s0 + lane * 8; v < s1; v += 256) {
-            float zt[8], zd[8];
-            load8(trow, P.dtype, s1, v, vec, zt);
-            load8(drow, P.dtype, s1, v, vec, zd);
+          if (kS && seg / kTreeChunk <= kTreeMaxChunkSums) {
+            // rows in shared memory: every 256-token chunk's sum, then one
+            // warp finds the crossing chunk (double-float prefix) and walks it
+            const int ncw = seg / kTreeChunk;
+            for (int ci = 0; ci < ncw; ++ci) {
+              const int v = s0 + ci * kTreeChunk + lane * 8;
+              float cs = 0.f;
+              if (v < s1) {
+                float zt[8], zd[8];
+                load8<kS>(trow, P.dtype, s1, v, vec, zt);
+                load8<kS>(drow, P.dtype, s1, v, vec, zd);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ws += D.pjz(zt[e], D.qz(zd[e]));
-          }
-          ws = warp_sum(ws);
-          __syncthreads();
-          if (lane == 0) s_seg[warp] = (double)ws;
-          __syncthreads();
-          if (warp == 0) {
-            double tot = 0.0;
-            for (int w = 0; w < kTreeWarps; ++w) tot += s_seg[w];
-            const double T = (double)u * tot;
-            double run = 0.0;
-            int wseg = -1, last = -1;
-            for (int w = 0; w < kTreeWarps; ++w) {
-              if (s_seg[w] > 0.0) last = w;
-              if (wseg < 0 && run + s_seg[w] > T) wseg = w;
-              if (wseg < 0) run += s_seg[w];
+                for (int e = 0; e < 8; ++e) cs += v + e < s1 ? D.pjz(zt[e], D.qz(zd[e])) : 0.f;
+              }
+              cs = warp_sum(cs);
+              if (lane == 0) s_csum[warp * ncw + ci] = cs;
             }
-            if (wseg < 0) {  // u * R at the total by rounding: the last segment with mass
-              wseg = last < 0 ? 0 : last;
-              run = tot - (last < 0 ? 0.0 : s_seg[wseg]);
-            }
-            const int a0 = min(V, wseg * seg), a1 = min(V, a0 + seg);
-            int found = -1, lastv = -1;
-            for (int cb = a0; cb < a1 && found < 0; cb += kTreeChunk) {
-              float pr[8], zt[8], zd[8];
-              float lsum = 0.f;
-              load8(trow, P.dtype, a1, cb + lane * 8, vec, zt);
-              load8(drow, P.dtype, a1, cb + lane * 8, vec, zd);
+            __syncthreads();
+            if (warp == 0) {
+              const int nc = kTreeWarps * ncw;
+              const int q = (nc + 31) / 32;
+              const int ja = min(nc, lane * q), jb = min(nc, ja + q);
+              DF mine = {0.f, 0.f};
+              for (int j = ja; j < jb; ++j) mine = df_add_f(mine, s_csum[j]);
+              const DF incl = warp_incl_scan_df(mine, lane);
+              DF tot;
+              tot.hi = __shfl_sync(0xffffffffu, incl.hi, 31);
+              tot.lo = __shfl_sync(0xffffffffu, incl.lo, 31);
+              const DF T = df_scale(u, tot);
+              DF run = df_add(incl, {-mine.hi, -mine.lo});
+              int cand = INT_MAX, lastc = -1;
+              DF pe = {0.f, 0.f};
+              for (int j = ja; j < jb; ++j) {
+                const float sj = s_csum[j];
+                if (sj > 0.f) lastc = j;
+                const DF nxt = df_add_f(run, sj);
+                if (cand == INT_MAX && df_gt(nxt, T)) {
+                  cand = j;
+                  pe = run;
+                }
+                run = nxt;
+              }
+              int jstar = warp_min_i(cand);
+              DF pexcl;
+              if (jstar != INT_MAX) {
+                const int owner = __ffs(__ballot_sync(0xffffffffu, cand == jstar)) - 1;
+                pexcl.hi = __shfl_sync(0xffffffffu, pe.hi, owner);
+                pexcl.lo = __shfl_sync(0xffffffffu, pe.lo, owner);
+              } else {  // u * R at the total by rounding: the last chunk with mass
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) lastc = max(lastc, __shfl_xor_sync(0xffffffffu, lastc, o));
+                jstar = lastc < 0 ? 0 : lastc;
+                pexcl = df_add_f(tot, -s_csum[jstar]);
+              }
+              // chunk jstar = warp (jstar / ncw)'s chunk (jstar % ncw)
+              const int cw = jstar / ncw, cc = jstar - cw * ncw;
+              const int c0 = min(V, cw * seg), c1 = min(V, c0 + seg);
+              const int v0 = c0 + cc * kTreeChunk + lane * 8;
+              float pr[8];
+              {
+                float zt[8], zd[8];
+                load8<kS>(trow, P.dtype, c1, v0, vec, zt);
+                load8<kS>(drow, P.dtype, c1, v0, vec, zd);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) pr[e] = v0 + e < c1 ? D.pjz(zt[e], D.qz(zd[e])) : 0.f;
+              }
+              float pre[8];
+              pre[0] = pr[0];
+#pragma unroll
+              for (int e = 1; e < 8; ++e) pre[e] = pre[e - 1] + pr[e];
+              const DF incl2 = warp_incl_scan_df({pre[7], 0.f}, lane);
+              const DF base = df_add(pexcl, df_add_f(incl2, -pre[7]));
+              int c2 = INT_MAX, back = -1;
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                const int v = cb + lane * 8 + e;
-                pr[e] = v < a1 ? D.pjz(zt[e], D.qz(zd[e])) : 0.f;
-                lsum += pr[e];
-                if (pr[e] > 0.f) lastv = max(lastv, v);
+                if (c2 == INT_MAX && pr[e] > 0.f && df_gt(df_add_f(base, pre[e]), T)) c2 = v0 + e;
+                if (pr[e] > 0.f) back = v0 + e;
               }
-              // inclusive prefix of the lane sums across the warp (fp64)
-              double incl = (double)lsum;
+              c2 = warp_min_i(c2);
 #pragma unroll
-              for (int o = 1; o < 32; o <<= 1) {
-                const double n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-              }
-              double pre = run + incl - (double)lsum;
-              int cand = INT_MAX;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                pre += (double)pr[e];
-                if (cand == INT_MAX && pr[e] > 0.f && pre > T) cand = cb + lane * 8 + e;
-              }
-              cand = warp_min_i(cand);
-              if (cand != INT_MAX) found = cand;
-              run += __shfl_sync(0xffffffffu, incl, 31);
+              for (int o = 16; o > 0; o >>= 1) back = max(back, __shfl_xor_sync(0xffffffffu, back, o));
+              if (lane == 0) s_tok = c2 != INT_MAX ? c2 : (back >= 0 ? back : 0);
             }
+          } else {
+            float ws = 0.f;
+            for (int v = s0 + lane * 8; v < s1; v += 256) {
+              float zt[8], zd[8];
+              load8<kS>(trow, P.dtype, s1, v, vec, zt);
+              load8<kS>(drow, P.dtype, s1, v, vec, zd);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) lastv = max(lastv, __shfl_xor_sync(0xffffffffu, lastv, o));
-            if (lane == 0) s_tok = found >= 0 ? found : (lastv >= 0 ? lastv : 0);
+              for (int e = 0; e < 8; ++e) ws += D.pjz(zt[e], D.qz(zd[e]));
+            }
+            ws = warp_sum(ws);
+            __syncthreads();
+            if (lane == 0) s_seg[warp] = (double)ws;
+            __syncthreads();
+            if (warp == 0) {
+              double tot = 0.0;
+              for (int w = 0; w < kTreeWarps; ++w) tot += s_seg[w];
+              const double T = (double)u * tot;
+              double run = 0.0;
+              int wseg = -1, last = -1;
+              for (int w = 0; w < kTreeWarps; ++w) {
+                if (s_seg[w] > 0.0) last = w;
+                if (wseg < 0 && run + s_seg[w] > T) wseg = w;
+                if (wseg < 0) run += s_seg[w];
+              }
+              if (wseg < 0) {  // u * R at the total by rounding: the last segment with mass
+                wseg = last < 0 ? 0 : last;
+                run = tot - (last < 0 ? 0.0 : s_seg[wseg]);
+              }
+              const int a0 = min(V, wseg * seg), a1 = min(V, a0 + seg);
+              int found = -1, lastv = -1;
+              for (int cb = a0; cb < a1 && found < 0; cb += kTreeChunk) {
+                float pr[8], zt[8], zd[8];
+                float lsum = 0.f;
+                load8<kS>(trow, P.dtype, a1, cb + lane * 8, vec, zt);
+                load8<kS>(drow, P.dtype, a1, cb + lane * 8, vec, zd);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int v = cb + lane * 8 + e;
+                  pr[e] = v < a1 ? D.pjz(zt[e], D.qz(zd[e])) : 0.f;
+                  lsum += pr[e];
+                  if (pr[e] > 0.f) lastv = max(lastv, v);
+                }
+                // inclusive prefix of the lane sums across the warp (fp64)
+                double incl = (double)lsum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                  const double n = __shfl_up_sync(0xffffffffu, incl, o);
+                  if (lane >= o) incl += n;
+                }
+                double pre = run + incl - (double)lsum;
+                int cand = INT_MAX;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  pre += (double)pr[e];
+                  if (cand == INT_MAX && pr[e] > 0.f && pre > T) cand = cb + lane * 8 + e;
+                }
+                cand = warp_min_i(cand);
+                if (cand != INT_MAX) found = cand;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+              }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) lastv = max(lastv, __shfl_xor_sync(0xffffffffu, lastv, o));
+              if (lane == 0) s_tok = found >= 0 ? found : (lastv >= 0 ? lastv : 0);
+            }
           }
           __syncthreads();
           if (tid == 0) out[depth] = s_tok;
@@ -386,7 +589,7 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
         }
       }
       if (tid == 0) {
-        out[depth] = __ldg(tok + next);
+        out[depth] = s_tokn[next];
         if (path) path[depth] = next;
       }
       cur = next;
@@ -426,7 +629,23 @@ extern "C" sv_status_t sv_verify_tree(int B, int N, int V, sv_dtype_t dtype, con
   if (ds != SV_OK) return ds;
   TreeParams P{B, N, V, (int)dtype, target_logits, draft_logits, tokens, parents, n_nodes, temperature, seed,
                out_tokens, out_accept_len, out_path, out_flags};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // both rows of a node staged in shared memory when they fit (one CTA per
+  // SM then); else the passes read them from L2
+  const size_t row_bytes = (size_t)V * esz;
+  const size_t smem = 2 * ((row_bytes + 127) / 128 * 128);
+  int dev = 0, optin = 0;
+  const bool aligned16 = row_bytes % 16 == 0 && host_aligned(target_logits, 16) && host_aligned(draft_logits, 16);
+  if (aligned16 && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+      smem + 1024 <= (size_t)optin &&
+      cudaFuncSetAttribute(tree_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess) {
+    const int grid = B < sms ? B : sms;
+    tree_kernel<true><<<grid, kTreeThreads, smem, st>>>(P);
+    return host_cuda_status(cudaGetLastError());
+  }
+  cudaGetLastError();
   const int grid = B < 2 * sms ? B : 2 * sms;
-  tree_kernel<<<grid, kTreeThreads, 0, static_cast<cudaStream_t>(stream)>>>(P);
+  tree_kernel<false><<<grid, kTreeThreads, 0, st>>>(P);
   return host_cuda_status(cudaGetLastError());
 }

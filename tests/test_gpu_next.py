@@ -223,6 +223,12 @@ def test_tree_parity_vocab_32000_sampled():
     _tree_compare(w, 3, idx=np.arange(0, 96, 6))
 
 
+def test_tree_parity_vocab_128256_rows_from_l2():
+    # two 256 KB rows per node do not fit in shared memory: every pass reads them from L2
+    w = synth.tree(seed=11, B=8, V=128256)
+    _tree_compare(w, 5)
+
+
 def test_tree_chain_equals_sv_verify():
     dev = torch.device("cuda")
     w = synth.c2(seed=7, device=dev)
