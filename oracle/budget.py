@@ -9,7 +9,7 @@ requests plus the sum of the n largest survivals, and the budget is the n
 that maximises that estimate divided by the measured cost of drafting and
 verifying n tokens; the n best-ranked drafts are kept.
 
-Readings where the page leaves a step open (also listed in the design doc):
+Readings where the page leaves a step open:
   - the survivals are the running product of the fp32 confidences, taken in
     fp32 in position order (the same precision as the kernel, so that the
     ranking -- an integer decision -- is identical on both sides);

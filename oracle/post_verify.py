@@ -12,7 +12,7 @@ Sources:
     grows by one entry per accepted draft and, at the first rejection, is cut
     back to the prefix length plus the number of emitted tokens.
 
-Readings (also listed in the design doc):
+Readings:
   - the verify input row of request b is in[b] = [t_last, d_0, ..., d_{K-1}]
     (the last committed token, then the drafts); the emitted tokens are
     out[b][0..a] (a accepted drafts, then the correction or bonus token);

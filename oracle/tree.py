@@ -12,7 +12,7 @@ Sources:
     rejection sample the normalised positive residual, and a bonus token when
     everything was accepted; its lesson table lists a tree verification mask.
 
-Readings (also listed in the design doc):
+Readings:
   - a request's tree has N nodes in topological order; node 0 is the last
     committed token, node n >= 1 carries draft token tok[n] and parent
     par[n] < n; children are tried in ascending node order;

@@ -7,7 +7,7 @@ takes a gradient step on L(q) = KL~(p || q) + lambda KL~(q_t || q) over the
 canvas, with position weights w_k favouring early positions; p is the target
 (teacher), q the draft being trained (student), q_t the draft as it was.
 
-Readings (also listed in the design doc):
+Readings:
   - KL~ over the canvas is the w_k-weighted per-position KL divergence over the
     whole vocabulary; the signal is computed at q = q_t, where the second
     term and its gradient vanish;
