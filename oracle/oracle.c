@@ -29,7 +29,7 @@
  *  [PX]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *        1, 2, 3" (SC'11) -- the Philox4x32-10 block function.
  *
- * Readings where the pages are silent (the same list is kept in the design doc):
+ * Readings where the pages are silent:
  *  - temperature tau divides both target and draft logits; tau == 0 is a
  *    greedy row (argmax matching, lowest index on ties, no uniforms drawn);
  *    a greedy row's distributions (for the AV feature) use tau = 1;
