@@ -1000,9 +1000,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
         Raw8 zd;
         zd.a = zd.b = make_uint4(0, 0, 0, 0);
         if (t.kind == kTaskResidual) zd = smem_raw8<kDtype>(S.ring[s] + kSampleHalfBytes, off);
-        float r[8];
-        weights_from<kDtype>(t, t.kind, off, n, zt, zd, r);
-        const float sm = warp_sum(sum8(r));
+        const float sm = warp_sum(weights_sum8<kDtype>(t, t.kind, off, n, zt, zd));
         if (lane == 0) sub[q] = sm;
       }
       const bool last = (h.flags & kFlagLast) != 0;

@@ -112,6 +112,55 @@ __device__ __forceinline__ void weights_from(const SampleTask &t, int kind, int 
   }
 }
 
+// The sum of the weights of the eight elements v0..v0+7, two elements per
+// packed fp32x2 instruction (each lane the same operations as weights_from).
+template <int kDtype>
+__device__ __forceinline__ float weights_sum8(const SampleTask &t, int kind, int v0, int V, const Raw8 &zt,
+                                              const Raw8 &zd) {
+  const float2 cc = make_float2(t.c, t.c), nb = make_float2(t.nbt, t.nbt);
+  float2 acc = make_float2(0.f, 0.f);
+  if (kind == kTaskResidual) {
+    const float2 it = make_float2(t.invtau, t.invtau), kh = make_float2(t.k0_hi, t.k0_hi);
+    const float2 kl = make_float2(t.k0_lo, t.k0_lo), l2e = make_float2(kLog2e, kLog2e);
+    const float2 c7 = make_float2(1.f / 5040.f, 1.f / 5040.f), c6 = make_float2(1.f / 720.f, 1.f / 720.f);
+    const float2 c5 = make_float2(1.f / 120.f, 1.f / 120.f), c4 = make_float2(1.f / 24.f, 1.f / 24.f);
+    const float2 c3 = make_float2(1.f / 6.f, 1.f / 6.f), c2 = make_float2(0.5f, 0.5f), one = make_float2(1.f, 1.f);
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+      const float2 a = make_float2(raw_at<kDtype>(zt, k), raw_at<kDtype>(zt, k + 1));
+      const float2 b = make_float2(raw_at<kDtype>(zd, k), raw_at<kDtype>(zd, k + 1));
+      float2 p = __ffma2_rn(a, cc, nb);
+      p.x = ex2_approx(p.x);
+      p.y = ex2_approx(p.y);
+      const float2 d = __fadd2_rn(__ffma2_rn(__fadd2_rn(b, make_float2(-a.x, -a.y)), it, kh), kl);
+      float2 q = c7;  // -(e^d - 1) by the truncated Taylor series (one_minus_exp_small)
+      q = __ffma2_rn(q, d, c6);
+      q = __ffma2_rn(q, d, c5);
+      q = __ffma2_rn(q, d, c4);
+      q = __ffma2_rn(q, d, c3);
+      q = __ffma2_rn(q, d, c2);
+      q = __ffma2_rn(q, d, one);
+      const float2 sm = __fmul2_rn(q, d);
+      float2 ex = __fmul2_rn(d, l2e);
+      ex.x = ex2_approx(ex.x);
+      ex.y = ex2_approx(ex.y);
+      const float omx = d.x > -0.25f ? -sm.x : 1.f - ex.x, omy = d.y > -0.25f ? -sm.y : 1.f - ex.y;
+      const float wx = (p.x > 0.f && d.x < 0.f && v0 + k < V) ? p.x * omx : 0.f;
+      const float wy = (p.y > 0.f && d.y < 0.f && v0 + k + 1 < V) ? p.y * omy : 0.f;
+      acc = __fadd2_rn(acc, make_float2(wx, wy));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+      float2 p = __ffma2_rn(make_float2(raw_at<kDtype>(zt, k), raw_at<kDtype>(zt, k + 1)), cc, nb);
+      p.x = v0 + k < V ? ex2_approx(p.x) : 0.f;
+      p.y = v0 + k + 1 < V ? ex2_approx(p.y) : 0.f;
+      acc = __fadd2_rn(acc, p);
+    }
+  }
+  return acc.x + acc.y;
+}
+
 template <int kDtype>
 __device__ __forceinline__ void weights8(const SampleParams &P, const SampleTask &t, int kind, const RowPtrs &R, int j,
                                          int lane, float (&r)[8]) {
