@@ -256,9 +256,7 @@ __device__ __forceinline__ void group_sums(const SampleParams &P, const SampleTa
 #pragma unroll
   for (int u = 0; u < kSampleUnroll; ++u) {
     if (j0 + u < j1) {
-      float r[8];
-      weights_from<kDtype>(t, kind, (j0 + u) * kSubChunk + lane * 8, P.V, zt[u], zd[u], r);
-      const float s = warp_sum(sum8(r));
+      const float s = warp_sum(weights_sum8<kDtype>(t, kind, (j0 + u) * kSubChunk + lane * 8, P.V, zt[u], zd[u]));
       if (lane == 0) subsum[j0 + u] = s;
     }
   }
