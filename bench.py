@@ -196,7 +196,9 @@ def run_gpu(args):
     binding.lib()  # fails loudly if the library was not built
     cfg = WORKLOADS[args.workload]
     B, K, V = cfg["B"], cfg["K"], cfg["V"]
-    w = getattr(synth, args.workload)(seed=rank, device=dev)
+    if args.batch:  # a smaller batch of the same rows (profiler captures)
+        B = args.batch
+    w = getattr(synth, args.workload)(seed=rank, B=B, device=dev)
     theta0 = [1.0] + [0.0] * K if args.workload != "c5" else [0.55] + [0.9 - 0.15 * i for i in range(K)]
     theta = torch.tensor(theta0, dtype=torch.float32, device=dev)
     ws = binding.workspace(B, K, V, dev)
@@ -303,7 +305,8 @@ def run_gpu(args):
                            achieved_gbs=bytes_all / args.steps / (elapsed_ms / args.steps / 1e3) / 1e9)
     res["gpu_launches"] = launches_per_step * args.steps
     res["clocks"] = clk
-    res["config"] = dict(workload=args.workload + ": " + cfg["desc"], B=B, K=K, V=V, logits="bf16",
+    res["config"] = dict(workload=args.workload + ": " + cfg["desc"] + (" [batch %d]" % B if args.batch else ""),
+                         B=B, K=K, V=V, logits="bf16",
                          global_batch=B * world, l2="inputs %.0f MB per step > 129 MB L2: no flush" %
                          (w.bytes_first_pass() / 1e6), parallelism="replicas" if world > 1 else "single GPU")
     if rank == 0 and world == 1 and not args.no_e2e:
@@ -591,6 +594,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="c3")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences per step instead of the workload's B (for profiler captures on a small case)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
