@@ -112,7 +112,6 @@ struct NodeDist {
   float a, invZ;
   __device__ __forceinline__ float p0z(float zt) const { return ex2_approx((zt - Mt) * c) * inv_St; }
   __device__ __forceinline__ float qz(float zd) const { return ex2_approx((zd - Md) * c) * inv_Sd; }
-  __device__ __forceinline__ float p0(int v) const { return p0z(logit<kS>(trow, dtype, v)); }
   __device__ __forceinline__ float q(int v) const { return qz(logit<kS>(drow, dtype, v)); }
   // p_j(v) for j = nrej (the current residual) and the un-normalised
   // max(p_j - q, 0) for the next step
