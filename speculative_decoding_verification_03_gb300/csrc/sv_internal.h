@@ -21,6 +21,7 @@ constexpr int kPartSlots = 8;                      // finished items the math wa
 constexpr int kRowThreads = kConsumers + 32 + 32 * kEpiWarps;  // + producer warp + epilogue warps
 constexpr int kVecPerStage = kStageBytes / 16;     // 3072 16-byte vectors
 constexpr int kVecPerThread = kVecPerStage / kConsumers;  // 8
+static_assert(kVecPerStage % kConsumers == 0, "a stage is a whole number of vectors per math thread");
 constexpr int kMaxChunks = 16;                     // chunks a row may be split into
 constexpr int kChunkAlignElems = 512;              // chunk starts stay 16-byte aligned within a row
 
