@@ -11,16 +11,22 @@
 // sampling task for the residual or bonus row.
 //
 // GB300 design: a persistent grid, one CTA per SM, warp-specialised:
-//   warp 8  (producer)  takes work items from a global ticket and streams the
-//                       row bytes with 1-D TMA bulk copies into an 8-stage
-//                       shared-memory ring (16 KB stages, mbarrier complete_tx);
-//   warps 0-7 (math)    read 16-byte vectors from shared memory, keep a
-//                       warp-uniform running max (bf16x2 max + shuffles) and
-//                       a per-lane sum of exp2 terms, exclude exactly one copy
-//                       of the max, and publish one partial per warp and item;
-//   warp 9  (epilogue)  combines the 8 partials, merges row chunks, counts
-//                       finished rows per sequence and runs the scan for the
-//                       sequence whose last row it completed.
+//   warp 12 (producer)    takes work items -- queued target rows and sample
+//                         items first, then static rows from a global
+//                         ticket -- and streams them with 1-D TMA bulk copies
+//                         into a 4-stage shared-memory ring (54 KB stages,
+//                         mbarrier complete_tx);
+//   warps 0-11 (math)     read 16-byte vectors from shared memory, keep a
+//                         warp-uniform running max (bf16x2 max + redux) and
+//                         a per-lane sum of exp2 terms (packed fp32x2),
+//                         exclude exactly one copy of the max, and publish one
+//                         partial per warp and item; sample stages sum the
+//                         residual / bonus weights per 256-element sub-chunk;
+//   warps 13-15 (epilogue) take finished items from a shared counter, combine
+//                         the 12 partials, merge row chunks, and run the
+//                         early-exit walk of the sequence whose row they
+//                         completed (decisions, AV scores and refit labels,
+//                         queueing the next target row or the draw).
 // Every wait is bounded (2 s by default); a time-out sets SV_FLAG_TIMEOUT,
 // drains this CTA's in-flight copies and returns.
 #include <cfloat>

@@ -12,15 +12,15 @@
 namespace sv {
 
 // ---- row pass geometry -----------------------------------------------------
-constexpr int kStageBytes = 49152;                 // one TMA bulk copy
-constexpr int kStages = 4;                         // ring depth (192 KB in flight per SM)
+constexpr int kStageBytes = 55296;                 // one TMA bulk copy (9 x 384 threads x 16 B)
+constexpr int kStages = 4;                         // ring depth (216 KB in flight per SM)
 constexpr int kConsumerWarps = 12;
 constexpr int kConsumers = kConsumerWarps * 32;    // 384 math threads
 constexpr int kEpiWarps = 3;                       // epilogue warps (take items from a shared counter)
 constexpr int kPartSlots = 8;                      // finished items the math warps may run ahead
 constexpr int kRowThreads = kConsumers + 32 + 32 * kEpiWarps;  // + producer warp + epilogue warps
-constexpr int kVecPerStage = kStageBytes / 16;     // 3072 16-byte vectors
-constexpr int kVecPerThread = kVecPerStage / kConsumers;  // 8
+constexpr int kVecPerStage = kStageBytes / 16;     // 3456 16-byte vectors
+constexpr int kVecPerThread = kVecPerStage / kConsumers;  // 9
 static_assert(kVecPerStage % kConsumers == 0, "a stage is a whole number of vectors per math thread");
 constexpr int kMaxChunks = 16;                     // chunks a row may be split into
 constexpr int kChunkAlignElems = 512;              // chunk starts stay 16-byte aligned within a row
