@@ -620,41 +620,21 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
     float cached_c = 1.f;
     bool ok = true;
     const int K = P.K;
-    // A static ticket is taken only when its item is staged (a ticket held
-    // while queued items go first would delay a row the decisions wait for).
+    // Static items first (every first target row and every draft row,
+    // position-major), then the queued items (target rows the decisions
+    // wait for, and the draws' sample items): measured faster than letting
+    // queued items go first, as the static rows stream without interleaving
+    // and the chains then advance on a machine that is no longer saturated.
     // Queued items are claimed with one atomicAdd each (a unique slot, no
-    // retries); a claimed slot whose entry is not yet published stays
-    // pending while static items continue, and is waited on (bounded) only
-    // when no static item is left.
+    // retries) and waited on (bounded) until published.
     bool static_left = true, dyn_left = P.fused != 0;
-    int pending = -1;   // claimed queue slot, not yet taken
-    int pend_val = 0;   // its entry as last read (one item ahead)
-    int q_head = 0, q_tail = 0;
-    if (P.fused) {
-      q_head = ld_relaxed_gpu(reinterpret_cast<const int *>(P.dq_head));
-      q_tail = ld_relaxed_gpu(reinterpret_cast<const int *>(P.dq_tail));
-    }
     for (;;) {
       int dyn = -1;
       int row_b = 0, row_chunk = 0, row_target = 0, row_pos = 0;
-      if (dyn_left) {
-        if (pending < 0 && (q_head < q_tail || !static_left)) {
-          const int c = (int)atomicAdd(P.dq_head, 1u);
-          if (c < P.ndyn) {
-            pending = c;
-            pend_val = ld_relaxed_gpu(P.dq + c);
-          } else {
-            dyn_left = false;
-          }
-        }
-        if (pending >= 0 && (pend_val != 0 || !static_left)) {
-          dyn = pending;  // published, or nothing else to do: wait for it below
-          pending = -1;
-        }
-        // queue state for the next decision, read while this item is staged
-        q_head = ld_relaxed_gpu(reinterpret_cast<const int *>(P.dq_head));
-        q_tail = ld_relaxed_gpu(reinterpret_cast<const int *>(P.dq_tail));
-        if (pending >= 0) pend_val = ld_relaxed_gpu(P.dq + pending);
+      if (!static_left && dyn_left) {
+        const int c = (int)atomicAdd(P.dq_head, 1u);
+        if (c < P.ndyn) dyn = c;
+        else dyn_left = false;
       }
       int item;
       if (dyn >= 0) {
