@@ -210,7 +210,7 @@ sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *targe
   P.fused = ((size_t)V * esz) % 16 == 0 && aligned(target_logits, 16) && (!draft_logits || aligned(draft_logits, 16));
   size_t clear = L.counters_off + L.counters_bytes;
   if (P.fused) {
-    int sp = (S.nsub + 127) / 128;
+    int sp = (S.nsub + 255) / 256;  // parts of up to 256 sub-chunks (measured: fewer, larger parts are faster)
     sp = sp < 1 ? 1 : (sp > kMaxSampleParts ? kMaxSampleParts : sp);
     P.sp = sp;
     P.spc = (S.nsub + sp - 1) / sp;
