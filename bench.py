@@ -54,7 +54,8 @@ def _peak():
 def _kernel_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_03_gb300", "csrc")
-    for fn in ("rowpass.cu", "api.cu", "sv_device.cuh", "sv_internal.h", "sample_common.cuh", "avfit_common.cuh"):
+    for fn in ("rowpass.cu", "api.cu", "rowstats.cuh", "sv_device.cuh", "sv_internal.h", "sample_common.cuh",
+               "avfit_common.cuh"):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
