@@ -241,8 +241,6 @@ sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *targe
       P.ndyn = B * sp;
     }
     P.pos_cnt = reinterpret_cast<uint32_t *>(w + L.pos_cnt_off);
-    P.t_req = reinterpret_cast<uint32_t *>(w + L.t_req_off);
-    P.enq_cnt = reinterpret_cast<uint32_t *>(w + L.enq_cnt_off);
     clear = L.dq_off + (size_t)P.ndyn * 4;
   }
 

@@ -334,19 +334,6 @@ __device__ void finish_verify(const RowPassParams &P, int b, int lane) {
 // position finish (fused verify modes).
 // ---------------------------------------------------------------------------
 
-// fp32 acceptance test of position i with the exact fp64 fallback (one lane).
-__device__ __forceinline__ bool reject_at(const RowPassParams &P, int b, int i, const Part &T, const Part &D,
-                                          float tau_f, bool greedy, int d, bool in_range) {
-  if (greedy) return !(in_range && d == T.arg);
-  if (!in_range) return true;
-  const float u = uniform24f(P.seed, (uint32_t)b, (uint32_t)i, 0);
-  const long long rowb = (long long)P.V;
-  const float zt = logit_at(P.target, P.dtype, ((long long)b * (P.K + 1) + i) * rowb + d);
-  const float zd = logit_at(P.draft, P.dtype, ((long long)b * P.K + i) * rowb + d);
-  return reject_values(u, zt, zd, T, D, tau_f);
-}
-
-
 // A sequence finished one of its theta-reading events (a draft row's score,
 // or the final decision).  The event that completes the last sequence of the
 // launch runs the refit round update (warp-wide).
@@ -369,6 +356,13 @@ __device__ void seq_event(const RowPassParams &P, int b, int k, int lane) {
     }
     av_round_update(P.av_state, P.theta_rw, P.K, P.round_len, P.damping_c, t, lane);
   }
+}
+
+// Target rows the walk queued when its accepted positions were 0..a-1 (see
+// rows_on_accept): rows 1..min(a + 1, k) with look-ahead, rows 1..a without.
+__device__ __forceinline__ int rows_queued(const RowPassParams &P, int a, int k) {
+  if (a == 0) return 0;
+  return P.spec ? min(a + 1, k) : a;
 }
 
 // The walk ended at position a (a < k: first rejection; a == k: all
@@ -434,15 +428,26 @@ __device__ void lazy_finalize(const RowPassParams &P, int b, int a, int k, int l
     t.u = greedy ? 0.0 : (double)uniform24f(P.seed, (uint32_t)b, (uint32_t)a, 1);
     P.tasks[b] = t;
     // the sample items (the task is visible first), then fillers for the
-    // target rows K - a that were never queued
+    // target rows that were never queued (every queued target row, including
+    // one queued ahead and not needed, counts against the sequence's K)
     __threadfence();
-    // every queued target row (including one queued ahead and not needed)
-    // counts against the sequence's K rows of queue
-    const int nfill = (K - (int)__ldcg(P.enq_cnt + b)) * P.nch_dyn;
+    const int nfill = (K - rows_queued(P, a, k)) * P.nch_dyn;
     const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)(P.sp + nfill));
     for (int q = 0; q < P.sp; ++q) st_relaxed_gpu(P.dq + base + q, b * P.sp + q + 1);
     for (int q = 0; q < nfill; ++q) st_relaxed_gpu(P.dq + base + P.sp + q, kQueueNop);
     P.out_accept_len[b] = a;
+  }
+  if (P.fit) {
+    // the labelled drafts (up to and including the first rejection) add
+    // their refit terms ("Fitting the coefficients"), one lane per position
+    const int nlab = min(a + 1, k);
+    if (lane < nlab) {
+      const Part D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + lane)
+                                      : load_stats_cg(st + 2 * lane + 1);
+      const float x = av_feature(D.E);
+      fit_label(P, lane, x, av_conf(P, lane, x), lane < a);
+    }
+    __syncwarp();  // the labels before seq_event's fence
   }
   flags = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0 && flags) atomicOr(P.status, flags);
@@ -450,57 +455,104 @@ __device__ void lazy_finalize(const RowPassParams &P, int b, int a, int k, int l
 }
 
 // Events of position i: reached (i >= 1: position i - 1 accepted), its target
-// row done, its draft row done (i < k).  The event that completes them
-// decides the position (or, at i == k, finalizes with the bonus row).
+// row done, its draft row done (i < k), each one atomicAdd on the position's
+// counter.  The event that completes them decides the position (or, at
+// i == k, finalizes with the bonus row), after a fence.
 __device__ __forceinline__ uint32_t pos_need(int i, int k) {
   return (i >= 1 ? 1u : 0u) + 1u + (i < k ? 1u : 0u);
 }
-// lane 0: one event of position i; true when it completed the position
-__device__ __forceinline__ bool pos_event(const RowPassParams &P, int b, int i, int k) {
-  const bool done = atomicAdd(P.pos_cnt + (size_t)b * (P.K + 1) + i, 1u) == pos_need(i, k) - 1u;
-  if (done) __threadfence();
-  return done;
+// Target rows queued when position i is accepted, [*j0, *j1] (empty when
+// j1 < j0).  Each row is queued exactly once, by a fixed rule: with
+// look-ahead (P.spec) the acceptance of position 0 queues rows 1 and 2 and
+// that of position i >= 1 row i + 2 (row i + 1 came with position i - 1);
+// without it the acceptance of position i queues row i + 1.
+__device__ __forceinline__ void rows_on_accept(const RowPassParams &P, int i, int k, int *j0, int *j1) {
+  if (!P.spec) {
+    *j0 = *j1 = i + 1;
+  } else if (i == 0) {
+    *j0 = 1;
+    *j1 = min(2, k);
+  } else {
+    *j0 = *j1 = i + 2;
+    if (i + 2 > k) *j1 = i + 1;
+  }
 }
-// lane 0: queue target row j of sequence b unless it is queued already
-__device__ __forceinline__ void queue_target(const RowPassParams &P, int b, int j) {
-  if (atomicExch(P.t_req + (size_t)b * (P.K + 1) + j, 1u) != 0u) return;
-  atomicAdd(P.enq_cnt + b, 1u);
-  const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)P.nch_dyn);
-  const int code0 = P.B * P.sp + (b * P.K + (j - 1)) * P.nch_dyn + 1;
-  for (int c = 0; c < P.nch_dyn; ++c) st_relaxed_gpu(P.dq + base + c, code0 + c);
+// lane 0: publish target rows j0..j1 of sequence b in the queue slots from base
+__device__ __forceinline__ void publish_targets(const RowPassParams &P, int b, int j0, int j1, uint32_t base) {
+  int q = 0;
+  for (int j = j0; j <= j1; ++j) {
+    const int code0 = P.B * P.sp + (b * P.K + (j - 1)) * P.nch_dyn + 1;
+    for (int c = 0; c < P.nch_dyn; ++c) st_relaxed_gpu(P.dq + base + q++, code0 + c);
+  }
 }
 
-// The walk from position i (all of whose events are in): test it; an
-// accepted position queues target row i + 1 and (P.spec) one step ahead row
-// i + 2, so the next link's row is often done by the time it is reached;
-// then it reaches i + 1, continuing while that position's rows are done.
-__device__ void lazy_walk(const RowPassParams &P, int b, int i, int k, int lane) {
+// Inputs of the decision at position i that no other row's completion
+// changes: the drafted token d and the two logits at it (loaded while the
+// position's event counter is updated, so that the latencies overlap).
+struct PosInputs {
+  int d;
+  float zt, zd;
+};
+__device__ __forceinline__ PosInputs pos_logits(const RowPassParams &P, int b, int i, int d) {
+  PosInputs in;
+  in.d = d;
+  in.zt = in.zd = 0.f;
+  if (in.d >= 0 && in.d < P.V) {
+    const long long rowb = (long long)P.V;
+    in.zt = logit_at(P.target, P.dtype, ((long long)b * (P.K + 1) + i) * rowb + in.d);
+    in.zd = logit_at(P.draft, P.dtype, ((long long)b * P.K + i) * rowb + in.d);
+  }
+  return in;
+}
+
+// fp32 acceptance test of position i with the exact fp64 fallback (one lane).
+__device__ __forceinline__ bool reject_in(const RowPassParams &P, int b, int i, const Part &T, const Part &D,
+                                          float tau_f, bool greedy, const PosInputs &in) {
+  const bool in_range = in.d >= 0 && in.d < P.V;
+  if (greedy) return !(in_range && in.d == T.arg);
+  if (!in_range) return true;
+  const float u = uniform24f(P.seed, (uint32_t)b, (uint32_t)i, 0);
+  return reject_values(u, in.zt, in.zd, T, D, tau_f);
+}
+
+// The walk from position i (all of whose events are in; `known` holds the
+// statistics of the row whose completion got here: sidx_known = 2 i (target)
+// or 2 i + 1 (draft), -1 when both rows must be loaded; `in` the position's
+// inputs).  An accepted position queues the rows of rows_on_accept, then
+// reaches i + 1, continuing while that position's rows are done.
+__device__ void lazy_walk(const RowPassParams &P, int b, int i, int k, int lane, const Part known, int sidx_known,
+                          PosInputs in) {
   const int K = P.K;
+  const float tau_f = __ldg(P.temperature + b);
+  const bool greedy = !(tau_f > 0.f);
   for (;;) {
     int rej = 0, cont = 0;
     if (lane == 0) {
       const sv_row_stats_t *st = P.stats + (size_t)b * (2 * K + 1);
-      const Part T = load_stats_cg(st + 2 * i);
-      const Part D = P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + i) : load_stats_cg(st + 2 * i + 1);
-      const float tau_f = __ldg(P.temperature + b);
-      const bool greedy = !(tau_f > 0.f);
-      const int d = __ldg(P.draft_tokens + (size_t)b * K + i);
-      const bool in_range = d >= 0 && d < P.V;
-      const bool reject = reject_at(P, b, i, T, D, tau_f, greedy, d, in_range);
+      const Part T = sidx_known == 2 * i ? known : load_stats_cg(st + 2 * i);
+      const Part D = sidx_known == 2 * i + 1 ? known
+                     : (P.draft_stats_in ? load_stats_cg(P.draft_stats_in + (size_t)b * K + i)
+                                         : load_stats_cg(st + 2 * i + 1));
+      const bool reject = reject_in(P, b, i, T, D, tau_f, greedy, in);
       if (T.flags & SV_FLAG_NONFINITE) atomicOr(P.status, SV_FLAG_NONFINITE);
-      if (!reject) {
-        queue_target(P, b, i + 1);                 // i + 1 <= k: on the critical path
-        if (P.spec && i + 2 <= k) queue_target(P, b, i + 2);  // speculative, one step ahead
-        P.out_tokens[(size_t)b * (K + 1) + i] = d;
-      }
-      if (P.fit) {
-        const float x = av_feature(D.E);
-        fit_label(P, i, x, av_conf(P, i, x), !reject);
-      }
       rej = reject;
       if (!reject) {
-        __threadfence();  // the queue count is read by whichever warp finalizes
-        cont = pos_event(P, b, i + 1, k);  // reached
+        // Issued in this order so that the round trips overlap: the next
+        // drafted token, the queue reservation for the next target rows, the
+        // "reached" event of position i + 1; then the queue entries (their
+        // slots are reserved, so a walk that races ahead cannot take them)
+        // and the logits at the next token.
+        P.out_tokens[(size_t)b * (K + 1) + i] = in.d;
+        const int dn = i + 1 < K ? __ldg(P.draft_tokens + (size_t)b * K + i + 1) : 0;
+        int j0, j1;
+        rows_on_accept(P, i, k, &j0, &j1);
+        uint32_t base = 0;
+        if (j1 >= j0) base = atomicAdd(P.dq_tail, (uint32_t)((j1 - j0 + 1) * P.nch_dyn));
+        const uint32_t old = atomicAdd(P.pos_cnt + (size_t)b * (K + 1) + i + 1, 1u);
+        if (j1 >= j0) publish_targets(P, b, j0, j1, base);
+        if (i + 1 < k) in = pos_logits(P, b, i + 1, dn);
+        cont = old == pos_need(i + 1, k) - 1u;
+        if (cont) __threadfence();
       }
     }
     rej = __shfl_sync(0xffffffffu, rej, 0);
@@ -511,6 +563,7 @@ __device__ void lazy_walk(const RowPassParams &P, int b, int i, int k, int lane)
     }
     if (!cont) return;
     ++i;
+    sidx_known = -1;
     if (i == k) {  // every draft accepted and the bonus row is done
       lazy_finalize(P, b, k, k, lane);
       return;
@@ -518,27 +571,36 @@ __device__ void lazy_walk(const RowPassParams &P, int b, int i, int k, int lane)
   }
 }
 
-// A row of sequence b finished (sidx = 2 i: target row i, 2 i + 1: draft row i).
-__device__ __noinline__ void lazy_row_done(const RowPassParams &P, int b, int sidx, int lane) {
+// A row of sequence b finished (sidx = 2 i: target row i, 2 i + 1: draft row
+// i); R (lane 0) holds its statistics, already stored.
+__device__ __noinline__ void lazy_row_done(const RowPassParams &P, int b, int sidx, const Part R, int lane) {
   const int k = kept_len_of(P, b);
   const int i = sidx >> 1;
   int ready = 0;
+  PosInputs in;
+  in.d = 0;
+  in.zt = in.zd = 0.f;
   if (lane == 0) {
-    const Part R = load_stats_cg(P.stats + (size_t)b * (2 * P.K + 1) + sidx);
+    // the drafted token and this row's event first, so that their round
+    // trips overlap each other and the work below
+    const int d = i < P.K ? __ldg(P.draft_tokens + (size_t)b * P.K + i) : 0;
+    const uint32_t old = atomicAdd(P.pos_cnt + (size_t)b * (P.K + 1) + i, 1u);
     // a draft row is always used (its AV score); a target row's flags are
     // raised when its position is decided (it may have been read ahead)
     if ((sidx & 1) && (R.flags & SV_FLAG_NONFINITE)) atomicOr(P.status, SV_FLAG_NONFINITE);
+    if (i < P.K) in = pos_logits(P, b, i, d);
     if ((sidx & 1) && (P.out_feature || P.out_conf)) {  // a draft row's score
       const float x = av_feature(R.E);
       if (P.out_feature) P.out_feature[(size_t)b * P.K + i] = x;
       if (P.out_conf) P.out_conf[(size_t)b * P.K + i] = av_conf(P, i, x);
     }
-    ready = pos_event(P, b, i, k);
+    ready = old == pos_need(i, k) - 1u;
+    if (ready) __threadfence();
   }
   ready = __shfl_sync(0xffffffffu, ready, 0);
   if (ready) {
     if (i == k) lazy_finalize(P, b, k, k, lane);  // every draft accepted: bonus from row k
-    else lazy_walk(P, b, i, k, lane);
+    else lazy_walk(P, b, i, k, lane, R, sidx, in);
   }
   if (sidx & 1) seq_event(P, b, k, lane);
 }
@@ -932,7 +994,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
       }
       seq_done = __shfl_sync(0xffffffffu, seq_done, 0);
       if (seq_done == 2) {
-        lazy_row_done(P, info.b, info.sidx, lane);
+        lazy_row_done(P, info.b, info.sidx, R, lane);
       } else if (seq_done) {
         __threadfence();
         if (P.mode == kScore) finish_score(P, info.b, lane);

@@ -133,9 +133,7 @@ struct RowPassParams {
   int nch_dyn;        // chunks of a queued target row (shortens the chain of decisions)
   int chunk_elems_dyn;
   uint32_t *pos_cnt;  // [B][K+1]: events of position i (reached, target row, draft row)
-  uint32_t *t_req;    // [B][K+1]: target row i queued
-  uint32_t *enq_cnt;  // [B]: target rows queued
-  int spec;           // queue target row i + 2 when position i is accepted
+  int spec;           // look-ahead: queue target row i + 2 when position i >= 1 is accepted
 };
 
 
@@ -144,7 +142,7 @@ constexpr int kMaxSampleParts = 16;
 
 struct WsLayout {
   size_t counters_off, counters_bytes;  // zeroed by every call
-  size_t ticket_off, fitacc_off, row_cnt_off, seq_cnt_off, smp_cnt_off, pos_cnt_off, t_req_off, enq_cnt_off, dq_off;
+  size_t ticket_off, fitacc_off, row_cnt_off, seq_cnt_off, smp_cnt_off, pos_cnt_off, dq_off;
   size_t stats_off, chunk_off, task_off, subsum_off;
   size_t total;
 };
@@ -169,10 +167,6 @@ inline WsLayout ws_layout(int B, int K, int V) {
   off += (size_t)B * 4;
   L.pos_cnt_off = off;
   off += (size_t)B * (K + 1) * 4;
-  L.t_req_off = off;
-  off += (size_t)B * (K + 1) * 4;
-  L.enq_cnt_off = off;
-  off += (size_t)B * 4;
   L.dq_off = off;  // last: a call clears only the entries it uses
   off += (size_t)B * (kMaxSampleParts + (size_t)K * kMaxChunks) * 4;
   off = align_up(off, 256);
