@@ -15,6 +15,7 @@ mathematics: none (see the test files ``tests/test_oracle_*.py``).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -35,15 +36,23 @@ FLAG_BAD_LEN = 8
 FLAG_BAD_TEMP = 16
 
 
+_CFLAGS = ["-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so next to it (gcc, no fast-math,
     no FMA contraction, so x86 and Arm give the same bits)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
-        cmd = ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
-        subprocess.run(cmd, check=True)
+        compile_source(_SRC, tmp)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc with the oracle's flags: one C source into a shared library."""
+    subprocess.run(["gcc"] + _CFLAGS + [src, "-o", out, "-lm"], check=True)
+    return out
 
 
 class _RowStats(ctypes.Structure):
@@ -51,36 +60,56 @@ class _RowStats(ctypes.Structure):
                 ("argmax", ctypes.c_int), ("nonfinite", ctypes.c_int)]
 
 
+def _bind(path: str):
+    """Load a compiled oracle and declare its functions' signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    lib.orc_philox4x32_10.argtypes = [P, P, P]
+    lib.orc_philox4x32_10.restype = None
+    lib.orc_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
+    lib.orc_uniform.restype = ctypes.c_double
+    lib.orc_row_stats.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.POINTER(_RowStats)]
+    lib.orc_row_stats.restype = None
+    lib.orc_feature.argtypes = [ctypes.c_double]
+    lib.orc_feature.restype = ctypes.c_double
+    lib.orc_conf.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double]
+    lib.orc_conf.restype = ctypes.c_double
+    lib.orc_kept_len.argtypes = [P, ctypes.c_int, ctypes.c_double]
+    lib.orc_kept_len.restype = ctypes.c_int
+    lib.orc_av_score.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P,
+                                 ctypes.c_double, P, P, P]
+    lib.orc_av_score.restype = None
+    lib.orc_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P,
+                               ctypes.c_uint64, P, P, P, P, P, P, P, P]
+    lib.orc_verify.restype = None
+    lib.orc_av_accumulate.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
+    lib.orc_av_accumulate.restype = None
+    lib.orc_av_solve_update.argtypes = [ctypes.c_int, P, P, P, ctypes.c_double, P, P]
+    lib.orc_av_solve_update.restype = ctypes.c_int
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P = ctypes.c_void_p
-            lib.orc_philox4x32_10.argtypes = [P, P, P]
-            lib.orc_philox4x32_10.restype = None
-            lib.orc_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
-            lib.orc_uniform.restype = ctypes.c_double
-            lib.orc_row_stats.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.POINTER(_RowStats)]
-            lib.orc_row_stats.restype = None
-            lib.orc_feature.argtypes = [ctypes.c_double]
-            lib.orc_feature.restype = ctypes.c_double
-            lib.orc_conf.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double]
-            lib.orc_conf.restype = ctypes.c_double
-            lib.orc_kept_len.argtypes = [P, ctypes.c_int, ctypes.c_double]
-            lib.orc_kept_len.restype = ctypes.c_int
-            lib.orc_av_score.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P,
-                                         ctypes.c_double, P, P, P]
-            lib.orc_av_score.restype = None
-            lib.orc_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P,
-                                       ctypes.c_uint64, P, P, P, P, P, P, P, P]
-            lib.orc_verify.restype = None
-            lib.orc_av_accumulate.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
-            lib.orc_av_accumulate.restype = None
-            lib.orc_av_solve_update.argtypes = [ctypes.c_int, P, P, P, ctypes.c_double, P, P]
-            lib.orc_av_solve_update.restype = ctypes.c_int
-            _lib = lib
+            _lib = _bind(build())
     return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Run the oracle's Python functions on another compiled copy of oracle.c
+    (the pin tests use this to check that planted mistakes are caught)."""
+    global _lib
+    prev = _load()
+    with _lock:
+        _lib = _bind(path)
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = prev
 
 
 def _ptr(a):

@@ -194,3 +194,19 @@ def test_early_exit_uses_no_target_row_past_the_first_rejection():
     assert np.array_equal(g["tokens"], g0["tokens"]) and np.array_equal(g["accept_len"], g0["accept_len"])
     assert np.array_equal(g["conf"], g0["conf"])
     assert (r["accept_len"] < w.K).sum() > w.B // 2  # most sequences had rows to skip
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_zero_draft_probability_accepts(dtype):
+    """A drafted token the drafter gave probability 0 (logit -inf) has ratio
+    +inf and is always accepted, as in the cheatsheet's loop; the bonus token
+    then follows the target row."""
+    B, K, V = 64, 3, 256
+    g = torch.Generator().manual_seed(11)
+    t = (torch.randn((B, K + 1, V), generator=g) * 2.0).to(dtype)
+    d = (torch.randn((B, K, V), generator=g) * 2.0)
+    toks = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    d.scatter_(2, toks.long().unsqueeze(-1), float("-inf"))
+    w = synth.Workload("qzero", B, K, V, dtype, t.contiguous(), d.to(dtype).contiguous(), toks, torch.ones(B))
+    g_out, r = _check(w, 21)
+    assert np.all(g_out["accept_len"] == K) and np.all(r["accept_len"] == K)

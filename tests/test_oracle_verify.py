@@ -264,3 +264,15 @@ def test_cdf_tie_picks_the_next_token():
     assert r["accept_len"][0] == 1
     assert r["tokens"][0, 1] == 1
     assert r["margin"][0] == 0.0  # flagged as a near-tie
+
+
+def test_zero_draft_probability_accepts():
+    # the cheatsheet's loop ("algorithm loop in code") sets the ratio to +inf
+    # when the drafter gave the drafted token probability 0: always accepted,
+    # whatever the uniform
+    tgt = np.zeros((1, 2, 2), np.float32)                  # p = [0.5, 0.5] in both rows
+    drf = np.array([[[0.0, -np.inf]]], np.float32)         # q = [1, 0]: token 1 has q = 0
+    for seed in range(64):
+        r = oracle.verify(tgt, drf, np.array([[1]], np.int32), np.ones(1, np.float32), seed)
+        assert r["accept_len"][0] == 1 and r["tokens"][0, 0] == 1
+        assert r["flags"][0] == 0
