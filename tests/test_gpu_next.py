@@ -46,6 +46,17 @@ def test_budget_parity(B, K):
     assert 0 < gb <= B * K
 
 
+def test_budget_exact_tie_takes_the_smallest_budget():
+    # est / cost is exactly 1 for n = 0, 1, 2: the first maximum, n = 0
+    dev = torch.device("cuda")
+    conf = torch.ones((2, 1), dtype=torch.float32)
+    dc, vc = torch.zeros(3), torch.tensor([2.0, 3.0, 4.0])
+    g_b, g_k = binding.av_budget(conf.to(dev), 2, dc.to(dev), vc.to(dev))
+    r = oracle.av_budget(conf.numpy(), 2, dc.numpy(), vc.numpy())
+    assert int(g_b.item()) == r["budget"] == 0
+    assert list(g_k.cpu().numpy()) == [0, 0]
+
+
 def test_budget_ragged_ties_and_edges():
     conf, dc, vc = synth.budget_inputs(300, 8, seed=3)
     conf[::7] = 0.5                       # many equal survivals: ties by index

@@ -111,3 +111,93 @@ def test_planted_mistake_is_caught(tmp_path, name, old, new):
     with oracle.using_library(lib):
         caught = _first_failure()
     assert caught is not None, "no pin fails with the mistake: " + name
+
+
+# ---------------------------------------------------------------------------
+# The steps around verification (oracle/budget.py, post_verify.py, tts.py,
+# tree.py): the same check, with the mutated module loaded in place of the
+# original and the package's entry point swapped for the mutant's.
+# ---------------------------------------------------------------------------
+import importlib.util  # noqa: E402
+
+import test_oracle_next as nx  # noqa: E402
+
+PY_BATTERY = {
+    "budget": [
+        ("budget brute force", lambda: nx.test_budget_brute_force_over_subsets(0)),
+        ("budget brute force 2", lambda: nx.test_budget_brute_force_over_subsets(1)),
+        ("budget constant cost", nx.test_budget_constant_cost_keeps_everything),
+        ("budget linear cost", lambda: nx.test_budget_linear_cost_closed_form(0.6, 10.0, 1.0, False)),
+        ("budget ragged rows", nx.test_budget_ragged_rows_and_survival_rounding),
+        ("budget tie", nx.test_budget_tie_takes_the_smallest_budget),
+    ],
+    "post_verify": [
+        ("post-verify hand-worked", nx.test_post_verify_hand_worked_cases),
+        ("post-verify cache loop", lambda: nx.test_post_verify_kv_matches_the_cheatsheet_loop(0)),
+        ("post-verify flags", nx.test_post_verify_flags),
+    ],
+    "tts": [
+        ("tts KL vs library", nx.test_tts_kl_against_library_and_identity),
+        ("tts gradient by finite differences", nx.test_tts_gradient_by_finite_differences),
+    ],
+    "tree": [
+        ("tree chain = linear", nx.test_tree_chain_equals_linear_verification),
+        ("tree greedy by hand", nx.test_tree_greedy_walk_by_hand),
+        ("tree lossless", lambda: nx.test_tree_walk_is_lossless(2)),
+    ],
+}
+PY_ENTRY = {"budget": ["av_budget", "survival"], "post_verify": ["post_verify"], "tts": ["tts_signal"],
+            "tree": ["verify_tree", "tree_uniform"]}
+
+PY_MUTANTS = [
+    ("budget", "ranking ascending", "cand.sort(key=lambda t: (-t[0], t[1]))", "cand.sort(key=lambda t: (t[0], t[1]))"),
+    ("budget", "estimate without the requests", "run = float(n_req)", "run = 0.0"),
+    ("budget", "last maximum", "ratio[n] > best)", "ratio[n] >= best)"),
+    ("budget", "survival not cumulative", "run = np.float32(run * c[b, i])", "run = np.float32(c[b, i])"),
+    ("budget", "draft_len ignored", "for i in range(int(kl[b]))", "for i in range(K)"),
+    ("post_verify", "unaccepted drafts not shifted", "nxt[b, j] = inp[b, j + 1]", "nxt[b, j] = inp[b, j]"),
+    ("post_verify", "bonus gets a cache entry", "kv[b] += (a + 1) if a < k else k", "kv[b] += a + 1"),
+    ("post_verify", "history misses the last token", "for j in range(a + 1):\n            pos", "for j in range(a):\n            pos"),
+    ("tts", "KL direction", "terms = np.where(p > 0, p * (lp - lq), 0.0)", "terms = np.where(q > 0, q * (lq - lp), 0.0)"),
+    ("tts", "gradient sign", "grad[b, k] = w[k] * (q - p) / tb", "grad[b, k] = w[k] * (p - q) / tb"),
+    ("tts", "gradient without 1/tau", "grad[b, k] = w[k] * (q - p) / tb", "grad[b, k] = w[k] * (q - p)"),
+    ("tts", "weights dropped", "kl[b, k] = w[k] * np.sum(terms)", "kl[b, k] = np.sum(terms)"),
+    ("tree", "no residual after a rejected child", "p = r / np.sum(r)", "p = p"),
+    ("tree", "final draw on word 0", "tree_uniform(seed, key, depth, 0, 1)", "tree_uniform(seed, key, depth, 0, 0)"),
+    ("tree", "ratio inverted", "ratio = np.inf if q[x] == 0 else p[x] / q[x]", "ratio = np.inf if q[x] == 0 else q[x] / p[x]"),
+]
+
+
+def _load_mutant(mod, source, tmp_path):
+    path = tmp_path / (mod + "_mutant.py")
+    path.write_text(source)
+    spec = importlib.util.spec_from_file_location("oracle._mutant_" + mod, str(path),
+                                                  submodule_search_locations=None)
+    m = importlib.util.module_from_spec(spec)
+    m.__package__ = "oracle"
+    spec.loader.exec_module(m)
+    return m
+
+
+def _py_first_failure(mod):
+    for name, pin in PY_BATTERY[mod]:
+        try:
+            pin()
+        except Exception as e:
+            return name, e
+    return None
+
+
+def test_unchanged_python_oracles_pass_their_battery():
+    for mod in PY_BATTERY:
+        assert _py_first_failure(mod) is None, mod
+
+
+@pytest.mark.parametrize("mod,name,old,new", PY_MUTANTS, ids=[m[0] + ": " + m[1] for m in PY_MUTANTS])
+def test_planted_mistake_in_python_oracle_is_caught(tmp_path, monkeypatch, mod, name, old, new):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), mod + ".py")).read()
+    assert src.count(old) == 1, "mutation site not unique: " + name
+    m = _load_mutant(mod, src.replace(old, new), tmp_path)
+    for fn in PY_ENTRY[mod]:
+        monkeypatch.setattr(oracle, fn, getattr(m, fn))
+    assert _py_first_failure(mod) is not None, "no pin fails with the mistake: " + name

@@ -70,6 +70,15 @@ def test_budget_linear_cost_closed_form(c, a, bcost, expect_all):
     assert r["budget"] == (B if expect_all else 0)
 
 
+def test_budget_tie_takes_the_smallest_budget():
+    # est / cost equal for every n (est = [2, 3, 4] over cost = [2, 3, 4], all
+    # exact): the budget is the first n attaining the maximum, n = 0
+    conf = np.ones((2, 1), np.float32)
+    r = oracle.av_budget(conf, 2, np.zeros(3, np.float32), np.array([2.0, 3.0, 4.0], np.float32))
+    assert list(r["ratio"]) == [1.0, 1.0, 1.0]
+    assert r["budget"] == 0 and list(r["kept_len"]) == [0, 0]
+
+
 def test_budget_ragged_rows_and_survival_rounding():
     rng = np.random.default_rng(9)
     conf = rng.uniform(0.3, 1.0, (6, 5)).astype(np.float32)
