@@ -143,6 +143,9 @@ size_t sv_workspace_bytes(int B, int K, int V);
  * Out-of-range drafted tokens set SV_FLAG_TOKEN_RANGE and are rejected.
  * NaN logits set SV_FLAG_NONFINITE; that sequence's outputs are unspecified
  * but in range.
+ * Target rows after a sequence's first rejection do not affect any output.
+ * When the draft rows are streamed (draft_stats == NULL) they are not read
+ * either, apart from at most one row read ahead, whose flags are ignored.
  * ---------------------------------------------------------------------- */
 sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype,
                       const void *target_logits, const void *draft_logits,
