@@ -43,6 +43,10 @@ WORKLOADS = {
 }
 
 
+def _dtype_name(dt):
+    return {"torch.bfloat16": "bf16", "torch.float32": "f32"}.get(str(dt), str(dt))
+
+
 def _peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -204,36 +208,39 @@ def run_gpu(args):
     theta = torch.tensor(theta0, dtype=torch.float32, device=dev)
     ws = binding.workspace(B, K, V, dev)
     state = binding.AVState(K, device=dev)
-    out = dict(tokens=torch.empty((B, K + 1), dtype=torch.int32, device=dev),
-               accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
-               feature=torch.empty((B, K), dtype=torch.float32, device=dev),
-               conf=torch.empty((B, K), dtype=torch.float32, device=dev))
+    # every timed step writes its outputs to buffers of its own (nothing is
+    # copied inside the timed region to keep the outcomes for the byte count)
+    nbuf = max(args.steps, args.warmup)
+    outs = [dict(tokens=torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                 accept_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                 feature=torch.empty((B, K), dtype=torch.float32, device=dev),
+                 conf=torch.empty((B, K), dtype=torch.float32, device=dev)) for _ in range(nbuf)]
     score = None
     if args.workload == "c5":
         score = dict(feature=torch.empty((B, K), dtype=torch.float32, device=dev),
                      conf=torch.empty((B, K), dtype=torch.float32, device=dev),
-                     kept_len=torch.empty((B,), dtype=torch.int32, device=dev),
                      stats=torch.empty((B, K, 4), dtype=torch.int32, device=dev))
+        kept = [torch.empty((B,), dtype=torch.int32, device=dev) for _ in range(nbuf)]
     stream = torch.cuda.current_stream(dev)
     # inputs that fit in L2 get it flushed before every timed step (256 MB
     # written), and the steps are then timed by events around each step alone
     first_pass = w.bytes_first_pass()
     flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev) if first_pass <= L2_BYTES else None
 
-    def step(i, record=None):
+    def step(i, seed):
+        out = outs[i]
         if score is not None:
+            score["kept_len"] = kept[i]
             binding.av_score(w.draft, w.temperature, theta, keep_threshold=0.3, want_stats=True, ws=ws, out=score)
-            binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, i, draft_len=score["kept_len"],
+            binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, seed, draft_len=kept[i],
                            theta=theta, draft_stats=score["stats"], want_feature=True, ws=ws, out=out,
                            av_state=state)
         else:
-            binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, i, theta=theta, want_feature=True,
+            binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, seed, theta=theta, want_feature=True,
                            ws=ws, out=out, av_state=state)
-        if record is not None:
-            record.append((out["accept_len"].clone(), None if score is None else score["kept_len"].clone()))
 
     for i in range(args.warmup):
-        step(10**6 + i)
+        step(i, 10**6 + i)
     rc, flags = binding.status(ws)
     if rc != 0:
         raise SystemExit("device status %d (flags %#x) after warm-up" % (rc, flags))
@@ -247,7 +254,6 @@ def run_gpu(args):
     if flush is not None:
         step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
-    outcomes = []
     clocks = Clocks(local) if rank == 0 else None
     time.sleep(0.3 if clocks else 0)
     if world > 1:
@@ -261,7 +267,7 @@ def run_gpu(args):
             _flush_l2(flush)
             step_ev[i][0].record(stream)
         binding.set_launch_events(*ev[i])
-        step(i, outcomes)
+        step(i, i)
         if step_ev is not None:
             step_ev[i][1].record(stream)
     binding.set_launch_events(None, None)
@@ -278,9 +284,9 @@ def run_gpu(args):
     # work done: verified rows (sum over sequences of k_b + 1) and algorithmic bytes
     esz = w.target.element_size()
     rows, bytes_rp, bytes_all, bytes_eager = 0, 0, 0, 0
-    for acc, kept in outcomes:
-        a = acc.cpu().numpy()
-        k = np.full(B, K) if kept is None else kept.cpu().numpy()
+    for i in range(args.steps):
+        a = outs[i]["accept_len"].cpu().numpy()
+        k = np.full(B, K) if score is None else kept[i].cpu().numpy()
         f, t, e = _bytes_per_step(args.workload, K, V, esz, k, a)
         rows += int((k + 1).sum())
         bytes_rp += f
@@ -295,26 +301,31 @@ def run_gpu(args):
 
     res = dict(metric=METRIC, value=value, unit="rows/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
                ms_per_step=elapsed_ms / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
-               dtype="f32", data="synthetic (seeded; stands in for the pages' model pairs and datasets)")
+               dtype=_dtype_name(w.target.dtype),
+               data="synthetic (seeded; stands in for the pages' model pairs and datasets)")
     peak, peak_kind = _peak()
     # on the AV-truncated canvas both row passes of a step record the same
     # event pair; the later (verify) launch is the one that stays bracketed
     rp_ms = sum(rowpass_ms) / len(rowpass_ms)
-    # algorithmic bytes: every verified row once, the residual or bonus row
-    # again, the small per-sequence arrays -- a fixed definition that does
-    # not depend on how much of it the kernel gets to skip
-    rp_bytes = bytes_eager / args.steps
-    achieved = rp_bytes / (rp_ms / 1e3) / 1e9
+    # algorithmic bytes: what the method must read -- target rows 0 .. a_b
+    # (the walk stops at the first rejection), every verified draft row (its
+    # AV score is an output), the residual or bonus row again, the small
+    # per-sequence arrays; fixed by each step's outcome
     ee_bytes = bytes_rp / args.steps
+    achieved = ee_bytes / (rp_ms / 1e3) / 1e9
+    # the count with every verified target row (k_b + 1 per sequence) read
+    # whatever the outcome: an equivalent rate, not a bandwidth
+    all_rows = bytes_eager / args.steps
+    srt = sorted(rowpass_ms)
     res["roofline"] = dict(bound="hbm", kernel="rowpass_kernel", achieved=achieved, peak=peak, unit="GB/s",
                            frac=achieved / peak, peak_source="%s (MEASURED_PEAKS hbm_gbs)" % peak_kind
                            if peak_kind == "measured" else "fallback 6.8 TB/s",
-                           traffic=_traffic(args.workload), algorithmic_bytes_per_launch=rp_bytes,
+                           traffic=_traffic(args.workload), algorithmic_bytes_per_launch=ee_bytes,
                            ms_per_launch=rp_ms,
-                           # the bytes the early-exit walk actually needs (no target
-                           # row past the first rejection), and the bandwidth on them
-                           early_exit_bytes_per_launch=ee_bytes,
-                           frac_early_exit_bytes=ee_bytes / (rp_ms / 1e3) / 1e9 / peak)
+                           ms_per_launch_p10_p50_p90=[srt[len(srt) // 10], srt[len(srt) // 2],
+                                                      srt[(9 * len(srt)) // 10]],
+                           all_verified_rows_bytes_per_launch=all_rows,
+                           equivalent_gbs_all_verified_rows=all_rows / (rp_ms / 1e3) / 1e9)
     res["step_hbm"] = dict(algorithmic_bytes_per_step=bytes_all / args.steps,
                            achieved_gbs=bytes_all / args.steps / (elapsed_ms / args.steps / 1e3) / 1e9)
     res["gpu_launches"] = launches_per_step * args.steps

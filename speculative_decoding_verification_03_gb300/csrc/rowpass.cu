@@ -949,20 +949,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.pempty[slot]);
       int seq_done = 0;
-      // Gather the 8 warp partials into lane 0 in warp order.
-      Part R;
-      R.m = __shfl_sync(0xffffffffu, mine.m, 0);
-      R.E = __shfl_sync(0xffffffffu, mine.E, 0);
-      R.arg = __shfl_sync(0xffffffffu, mine.arg, 0);
-      R.flags = __shfl_sync(0xffffffffu, mine.flags, 0);
-      for (int w = 1; w < kConsumerWarps; ++w) {
-        Part o;
-        o.m = __shfl_sync(0xffffffffu, mine.m, w);
-        o.E = __shfl_sync(0xffffffffu, mine.E, w);
-        o.arg = __shfl_sync(0xffffffffu, mine.arg, w);
-        o.flags = __shfl_sync(0xffffffffu, mine.flags, w);
-        R = combine(R, o, info.c);
-      }
+      // the math warps' partials, combined across this warp's lanes
+      Part R = combine_warp(mine, info.c);
       if (lane == 0) {
         const size_t row = (size_t)info.b * (2 * K + 1) + info.sidx;
         bool row_done = true;

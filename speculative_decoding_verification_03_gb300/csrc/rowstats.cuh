@@ -79,6 +79,29 @@ __device__ __forceinline__ Part combine(Part A, Part B, float c) {
   return W;
 }
 
+// The math warps' partials of one item, lane w holding warp w's (the other
+// lanes hold empty partials), combined across the warp.  The result is the
+// same as combining them one by one (up to rounding):
+//   M = the largest max; the winner = the lowest argmax attaining it;
+//   E = the winner's own sum plus, for every other partial,
+//       (E_w + 1) 2^((m_w - M) c), its maximum re-admitted as an ordinary
+//       element.
+// The exponentials are evaluated in parallel and summed in a fixed butterfly
+// order, so the item's latency does not grow with a chain of dependent
+// shuffles and MUFU operations (the pipes the math warps keep busy).
+// Warps cover disjoint elements, so argmaxes differ between partials.
+__device__ __forceinline__ Part combine_warp(const Part mine, float c) {
+  const bool empty = mine.arg == INT_MAX;
+  Part R;
+  R.flags = __reduce_or_sync(0xffffffffu, mine.flags | ((empty && isnan(mine.E)) ? (uint32_t)SV_FLAG_NONFINITE : 0u));
+  R.m = warp_max(empty ? -INFINITY : mine.m);
+  R.arg = warp_min_i((!empty && mine.m == R.m) ? mine.arg : INT_MAX);
+  float term = 0.f;
+  if (!empty) term = mine.arg == R.arg ? mine.E : (mine.E + 1.0f) * ex2_approx((mine.m - R.m) * c);
+  R.E = __shfl_sync(0xffffffffu, warp_sum(term), 0);
+  return R;
+}
+
 __device__ __forceinline__ float logit_at(const void *base, int dtype, long long idx) {
   if (dtype == SV_BF16) {
     const uint16_t h = __ldg(reinterpret_cast<const unsigned short *>(base) + idx);
