@@ -200,7 +200,9 @@ sv_status_t sv_av_score(int B, int K, int V, sv_dtype_t dtype,
  *
  *   theta       device float [K+1], read, and updated at round end
  *   av_state    device, >= sv_av_state_bytes(K)
- *   round_len   N >= 1 decode steps per refit
+ *   round_len   N >= 1 decode steps per refit; 0 = accumulate only, never
+ *               solve: the caller ends each round with sv_av_solve (the
+ *               sharded refit below)
  *   damping_c   constant of the damping n / (n + c), >= 0
  *   feature     device float [B][K] (from sv_verify or sv_av_score)
  *   accept_len  device int32 [B] (from sv_verify)
@@ -212,6 +214,41 @@ sv_status_t sv_av_fit_step(int B, int K, float *theta, void *av_state, size_t av
                            int round_len, float damping_c,
                            const float *feature, const int32_t *accept_len,
                            const int32_t *kept_len, void *stream);
+
+/* ------------------------------------------------------------------------
+ * The refit over a batch sharded across GPUs ("Adaptive Verification without
+ * a confidence head", section "Fitting the coefficients": one theta fitted
+ * from every label of the round, from gradient and Hessian sums of O(K^2)
+ * size).  The sums are additive over sequences, so a batch split over G
+ * GPUs reaches the single-GPU round update by one sum all-reduce of the
+ * accumulator block before the solve:
+ *   1. every GPU runs sv_av_fit_step or sv_verify_fit on its own sequences
+ *      with round_len = 0 (accumulate only);
+ *   2. at the round's end the caller sums the accumulator block of every
+ *      GPU's AV state in place (e.g. ncclAllReduce, ncclFloat64, ncclSum, on
+ *      av_state + sv_av_accum_offset(), sv_av_accum_bytes(K) / 8 values);
+ *   3. every GPU calls sv_av_solve with the same theta, and all get the same
+ *      update (identical fp64 inputs, identical arithmetic).
+ * With G = 1 this is exactly the round_len path.  Sums over G shards differ
+ * from the single-GPU sums only by the order of fp64 additions.
+ *
+ * sv_av_accum_offset()  byte offset of the block inside the AV state (a
+ *   multiple of 256).
+ * sv_av_accum_bytes(K)  its size: 4K + 2 fp64 values, in this order:
+ *   g[0] (slope), g[1..K] (intercepts), H_ww, H_wb[K], H_bb[K], n[K]
+ *   (H_wb[i] = sum of w x over position i's labels, H_bb[i] = sum of w,
+ *   n[i] = label count; w = s (1 - s)).  Returns 0 for K outside [0, 16].
+ * sv_av_solve -- end the round now: solve the arrow system from the block as
+ *   it stands, update theta as sv_av_fit_step does at a round's end
+ *   (damping n / (n + damping_c)), clear the block and the step counter.  A
+ *   round without labels leaves theta unchanged.  Asynchronous on `stream`;
+ *   SV_FLAG_FIT_SINGULAR in the AV state's status word as for
+ *   sv_av_fit_step.
+ * ---------------------------------------------------------------------- */
+size_t sv_av_accum_offset(void);
+size_t sv_av_accum_bytes(int K);
+sv_status_t sv_av_solve(int K, float *theta, void *av_state, size_t av_state_bytes, float damping_c,
+                        void *stream);
 
 /* ------------------------------------------------------------------------
  * sv_verify_fit -- sv_verify and one sv_av_fit_step in a single launch.

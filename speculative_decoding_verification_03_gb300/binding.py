@@ -90,6 +90,12 @@ def lib():
             L.sv_av_reset.restype = I
             L.sv_av_fit_step.argtypes = [I, I, P, P, SZ, I, F, P, P, P, P]
             L.sv_av_fit_step.restype = I
+            L.sv_av_accum_offset.argtypes = []
+            L.sv_av_accum_offset.restype = SZ
+            L.sv_av_accum_bytes.argtypes = [I]
+            L.sv_av_accum_bytes.restype = SZ
+            L.sv_av_solve.argtypes = [I, P, P, SZ, F, P]
+            L.sv_av_solve.restype = I
             L.sv_philox.argtypes = [U64, I, I, P, P]
             L.sv_philox.restype = I
             L.sv_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
@@ -249,6 +255,24 @@ class AVState:
                                   float(damping_c), _ptr(feature), _ptr(accept_len), _ptr(kept_len),
                                   _stream(stream))
         _check(rc, "sv_av_fit_step")
+
+    def accum(self) -> torch.Tensor:
+        """The round's accumulator block (sv_av_accum_offset / sv_av_accum_bytes):
+        a float64 view into the state, 4K + 2 values g[0..K], H_ww, H_wb[K],
+        H_bb[K], n[K].  Summing it over the shards of a batch (in place, e.g.
+        torch.distributed.all_reduce) before solve() gives the refit of the
+        whole batch."""
+        off = int(lib().sv_av_accum_offset())
+        n = int(lib().sv_av_accum_bytes(self.K))
+        return self.buf[off:off + n].view(torch.float64)
+
+    def solve(self, theta, damping_c: float = 10.0, stream=None):
+        """sv_av_solve: end the round now (solve from the accumulator block,
+        update theta in place, clear the block)."""
+        _dev(theta, "theta", torch.float32)
+        rc = lib().sv_av_solve(self.K, _ptr(theta), _ptr(self.buf), self.buf.numel(), float(damping_c),
+                               _stream(stream))
+        _check(rc, "sv_av_solve")
 
 
 class HostSession:

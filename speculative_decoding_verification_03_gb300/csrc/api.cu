@@ -13,6 +13,7 @@ cudaError_t launch_rowpass(const RowPassParams &P, int grid, cudaStream_t stream
 cudaError_t launch_sample(const SampleParams &P, int grid, cudaStream_t stream);
 cudaError_t launch_avfit(const FitParams &P, int grid, cudaStream_t stream);
 cudaError_t launch_philox(uint64_t seed, int nb, int npos, uint32_t *out, cudaStream_t stream);
+cudaError_t launch_avsolve(unsigned char *state, float *theta, int K, float damping_c, cudaStream_t stream);
 }  // namespace sv
 
 using namespace sv;
@@ -281,7 +282,7 @@ sv_status_t sv_verify_fit(int B, int K, int V, sv_dtype_t dtype, const void *tar
                           int32_t *out_accept_len, float *out_feature, float *out_conf, void *av_state,
                           size_t av_state_bytes, int round_len, float damping_c, void *workspace,
                           size_t workspace_bytes, void *stream) {
-  if (!theta || !aligned(theta, 4) || round_len < 1 || !(damping_c >= 0.f)) return SV_ERR_INVALID;
+  if (!theta || !aligned(theta, 4) || round_len < 0 || !(damping_c >= 0.f)) return SV_ERR_INVALID;
   if (K < 0 || K > SV_MAX_K) return SV_ERR_INVALID;
   if (!av_state || !aligned(av_state, 256) || av_state_bytes < sv_av_state_bytes(K)) return SV_ERR_WORKSPACE;
   if (B == 0)  // no sequences: the round still advances by one step
@@ -358,7 +359,7 @@ sv_status_t sv_av_reset(int K, void *av_state, size_t av_state_bytes, void *stre
 sv_status_t sv_av_fit_step(int B, int K, float *theta, void *av_state, size_t av_state_bytes, int round_len,
                            float damping_c, const float *feature, const int32_t *accept_len, const int32_t *kept_len,
                            void *stream) {
-  if (B < 0 || B > kMaxB || K < 0 || K > SV_MAX_K || round_len < 1 || !(damping_c >= 0.f)) return SV_ERR_INVALID;
+  if (B < 0 || B > kMaxB || K < 0 || K > SV_MAX_K || round_len < 0 || !(damping_c >= 0.f)) return SV_ERR_INVALID;
   if (!theta || !aligned(theta, 4)) return SV_ERR_INVALID;
   if (B > 0 && K > 0 && (!feature || !accept_len)) return SV_ERR_INVALID;
   if (!aligned(feature, 4) || !aligned(accept_len, 4) || !aligned(kept_len, 4)) return SV_ERR_INVALID;
@@ -380,6 +381,24 @@ sv_status_t sv_av_fit_step(int B, int K, float *theta, void *av_state, size_t av
   if (grid < 1) grid = 1;
   if (grid > kFitMaxCtas) grid = kFitMaxCtas;
   return cuda_status(launch_avfit(F, grid, static_cast<cudaStream_t>(stream)));
+}
+
+size_t sv_av_accum_offset(void) { return kAvAccOff; }
+
+size_t sv_av_accum_bytes(int K) {
+  if (K < 0 || K > SV_MAX_K) return 0;
+  return (size_t)(4 * K + 2) * sizeof(double);
+}
+
+sv_status_t sv_av_solve(int K, float *theta, void *av_state, size_t av_state_bytes, float damping_c, void *stream) {
+  if (K < 0 || K > SV_MAX_K || !(damping_c >= 0.f)) return SV_ERR_INVALID;
+  if (!theta || !aligned(theta, 4)) return SV_ERR_INVALID;
+  if (!av_state || !aligned(av_state, 256) || av_state_bytes < sv_av_state_bytes(K)) return SV_ERR_WORKSPACE;
+  int sms = 0;
+  const sv_status_t ds = device_info(&sms);
+  if (ds != SV_OK) return ds;
+  return cuda_status(launch_avsolve(static_cast<unsigned char *>(av_state), theta, K, damping_c,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 sv_status_t sv_philox(uint64_t seed, int nb, int npos, uint32_t *out, void *stream) {

@@ -95,6 +95,14 @@ __global__ void avfit_kernel(const FitParams P) {
   if (lane == 0) hdr->cta_done = 0u;
 }
 
+// End of an externally managed round: solve from the accumulators as they
+// stand (for a batch sharded over several GPUs, the caller has replaced them
+// by their sum over the shards) and clear them.  One warp.
+__global__ void avsolve_kernel(unsigned char *state, float *theta, int K, float damping_c) {
+  const double t[kFitQ] = {0, 0, 0, 0, 0, 0};
+  av_round_update(state, theta, K, 1, damping_c, t, (int)threadIdx.x);
+}
+
 __global__ void philox_kernel(uint64_t seed, int nb, int npos, uint32_t *out) {
   const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (long long)nb * npos) return;
@@ -110,6 +118,11 @@ __global__ void philox_kernel(uint64_t seed, int nb, int npos, uint32_t *out) {
 cudaError_t launch_avfit(const FitParams &P, int grid, cudaStream_t stream) {
   const int block = 32 * (P.K > 0 ? P.K : 1);
   avfit_kernel<<<grid, block, 0, stream>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_avsolve(unsigned char *state, float *theta, int K, float damping_c, cudaStream_t stream) {
+  avsolve_kernel<<<1, 32, 0, stream>>>(state, theta, K, damping_c);
   return cudaGetLastError();
 }
 

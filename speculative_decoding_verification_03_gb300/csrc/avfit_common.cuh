@@ -33,7 +33,8 @@ __device__ __forceinline__ void av_round_update(unsigned char *state, float *the
   const double hww = __ldcg(Hww) + warp_sum_d(lane < K ? t[1] : 0.0);
   const uint32_t step = hdr->step + 1u;
   bool solved = false;
-  if ((int)step >= round_len) {
+  // round_len == 0: accumulate only; the caller ends the round (sv_av_solve)
+  if (round_len > 0 && (int)step >= round_len) {
     const double ntot = warp_sum_d(nn);
     const double trace = hww + warp_sum_d(hbb);
     if (ntot > 0.0) {

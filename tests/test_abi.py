@@ -44,6 +44,12 @@ def test_workspace_sizes(lib):
     assert a % 256 == 0 and a < 4 << 20
     assert lib.sv_workspace_bytes(1024, 16, 151936) > a
     assert lib.sv_av_state_bytes(5) > 0 and lib.sv_av_state_bytes(17) == 0
+    # the refit's accumulator block: 4K + 2 fp64 values inside the AV state
+    for K in (0, 1, 5, 16):
+        off, n = lib.sv_av_accum_offset(), lib.sv_av_accum_bytes(K)
+        assert off % 256 == 0 and n == (4 * K + 2) * 8
+        assert off + n <= lib.sv_av_state_bytes(K)
+    assert lib.sv_av_accum_bytes(-1) == 0 and lib.sv_av_accum_bytes(17) == 0
 
 
 def _verify(lib, B=2, K=2, V=64, dtype=1, tgt=0x10000, drf=0x20000, toks=0x30000, tau=0x40000, theta=None,
@@ -73,12 +79,17 @@ def test_host_argument_checks(lib):
     assert _verify(lib, wsb=16) == WORKSPACE
     assert _verify(lib, B=0) == 0                        # nothing to do
     P = ctypes.c_void_p
-    assert lib.sv_av_fit_step(4, 4, P(0x1000), P(0x2000), 1 << 20, 0, 10.0, P(0x3000), P(0x4000), None, None) == INVALID
+    assert lib.sv_av_fit_step(4, 4, P(0x1000), P(0x2000), 1 << 20, -1, 10.0, P(0x3000), P(0x4000), None, None) == INVALID
     assert lib.sv_av_fit_step(4, 4, P(0x1000), P(0x2000), 1 << 20, 1, -1.0, P(0x3000), P(0x4000), None, None) == INVALID
     assert lib.sv_av_fit_step(4, 4, P(0x1000), P(0x2000), 16, 1, 10.0, P(0x3000), P(0x4000), None, None) == WORKSPACE
     assert lib.sv_av_score(4, 4, 64, 1, P(0x1000), P(0x2000), None, 0.3, P(0x3000), P(0x4000), None, None,
                            P(0x100000), 1 << 20, None) == INVALID      # theta missing
     assert lib.sv_philox(0, -1, 4, P(0x1000), None) == INVALID
+    assert lib.sv_av_solve(17, P(0x1000), P(0x2000), 1 << 20, 10.0, None) == INVALID
+    assert lib.sv_av_solve(4, None, P(0x2000), 1 << 20, 10.0, None) == INVALID
+    assert lib.sv_av_solve(4, P(0x1000), P(0x2000), 1 << 20, -1.0, None) == INVALID
+    assert lib.sv_av_solve(4, P(0x1000), P(0x2000), 16, 10.0, None) == WORKSPACE
+    assert lib.sv_av_solve(4, P(0x1000), P(0x2010), 1 << 20, 10.0, None) == WORKSPACE
     assert lib.sv_status(None, None, None) == INVALID
 
 
