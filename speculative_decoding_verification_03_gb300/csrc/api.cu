@@ -231,7 +231,11 @@ sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *targe
       P.lazy = 1;
       P.ngroups = K + 1;
       P.nstatic = P.nitems = P.ngroups * B * P.nch;
-      P.ndyn = B * (sp + K * P.nch_dyn);
+      P.ndyn = B * sp;
+      P.ntq = B * K * P.nch_dyn;
+      P.tq = reinterpret_cast<int *>(w + L.tq_off);
+      P.tq_tail = P.ticket + 4;
+      P.tq_head = P.ticket + 5;
       // Reading target row i + 2 one step ahead costs the rows of positions
       // rejected at i + 1 and shortens each sequence's chain of decisions:
       // measured faster while the streamed rows are under ~1 GB (the chains,
@@ -242,13 +246,13 @@ sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *targe
       P.ndyn = B * sp;
     }
     P.pos_cnt = reinterpret_cast<uint32_t *>(w + L.pos_cnt_off);
-    clear = L.dq_off + (size_t)P.ndyn * 4;
+    clear = P.lazy ? L.tq_off + (size_t)P.ntq * 4 : L.dq_off + (size_t)P.ndyn * 4;
   }
 
   // status word (offset 0) and the per-call counters, in one clear
   cudaError_t e = cudaMemsetAsync(w, 0, clear, st);
   if (e != cudaSuccess) return SV_ERR_CUDA;
-  const long long tickets = (long long)P.nitems + (P.fused ? P.ndyn : 0);
+  const long long tickets = (long long)P.nitems + (P.fused ? P.ndyn : 0) + P.ntq;
   const int grid = tickets < sms ? (int)tickets : sms;
   e = rowpass_timed(P, grid, st);
   if (e != cudaSuccess) return SV_ERR_CUDA;

@@ -427,14 +427,16 @@ __device__ void lazy_finalize(const RowPassParams &P, int b, int a, int k, int l
     }
     t.u = greedy ? 0.0 : (double)uniform24f(P.seed, (uint32_t)b, (uint32_t)a, 1);
     P.tasks[b] = t;
-    // the sample items (the task is visible first), then fillers for the
-    // target rows that were never queued (every queued target row, including
-    // one queued ahead and not needed, counts against the sequence's K)
+    // the sample items (the task is visible first), then fillers in the
+    // target-row queue for the rows that were never queued (every queued
+    // target row, including one queued ahead and not needed, counts against
+    // the sequence's K)
     __threadfence();
     const int nfill = (K - rows_queued(P, a, k)) * P.nch_dyn;
-    const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)(P.sp + nfill));
+    const uint32_t base = atomicAdd(P.dq_tail, (uint32_t)P.sp);
+    const uint32_t fbase = nfill > 0 ? atomicAdd(P.tq_tail, (uint32_t)nfill) : 0u;
     for (int q = 0; q < P.sp; ++q) st_relaxed_gpu(P.dq + base + q, b * P.sp + q + 1);
-    for (int q = 0; q < nfill; ++q) st_relaxed_gpu(P.dq + base + P.sp + q, kQueueNop);
+    for (int q = 0; q < nfill; ++q) st_relaxed_gpu(P.tq + fbase + q, kQueueNop);
     P.out_accept_len[b] = a;
   }
   if (P.fit) {
@@ -477,12 +479,13 @@ __device__ __forceinline__ void rows_on_accept(const RowPassParams &P, int i, in
     if (i + 2 > k) *j1 = i + 1;
   }
 }
-// lane 0: publish target rows j0..j1 of sequence b in the queue slots from base
+// lane 0: publish target rows j0..j1 of sequence b in the target-row queue
+// slots from base
 __device__ __forceinline__ void publish_targets(const RowPassParams &P, int b, int j0, int j1, uint32_t base) {
   int q = 0;
   for (int j = j0; j <= j1; ++j) {
-    const int code0 = P.B * P.sp + (b * P.K + (j - 1)) * P.nch_dyn + 1;
-    for (int c = 0; c < P.nch_dyn; ++c) st_relaxed_gpu(P.dq + base + q++, code0 + c);
+    const int code0 = (b * P.K + (j - 1)) * P.nch_dyn + 1;
+    for (int c = 0; c < P.nch_dyn; ++c) st_relaxed_gpu(P.tq + base + q++, code0 + c);
   }
 }
 
@@ -547,7 +550,7 @@ __device__ void lazy_walk(const RowPassParams &P, int b, int i, int k, int lane,
         int j0, j1;
         rows_on_accept(P, i, k, &j0, &j1);
         uint32_t base = 0;
-        if (j1 >= j0) base = atomicAdd(P.dq_tail, (uint32_t)((j1 - j0 + 1) * P.nch_dyn));
+        if (j1 >= j0) base = atomicAdd(P.tq_tail, (uint32_t)((j1 - j0 + 1) * P.nch_dyn));
         const uint32_t old = atomicAdd(P.pos_cnt + (size_t)b * (K + 1) + i + 1, 1u);
         if (j1 >= j0) publish_targets(P, b, j0, j1, base);
         if (i + 1 < k) in = pos_logits(P, b, i + 1, dn);
@@ -643,6 +646,30 @@ __device__ void finish_score(const RowPassParams &P, int b, int lane) {
 }
 
 // ---------------------------------------------------------------------------
+// Producer helpers: queue claims.
+// ---------------------------------------------------------------------------
+// The entry of a claimed slot (its publisher writes it right after the
+// reservation): wait (bounded) until it is nonzero.
+__device__ __forceinline__ bool wait_entry(const RowPassParams &P, const int *slot, volatile int *abort_flag,
+                                           int *out) {
+  int code = ld_acquire_gpu(slot);
+  if (code == 0) {
+    const uint64_t t0 = global_ns();
+    while ((code = ld_acquire_gpu(slot)) == 0) {
+      if (*abort_flag) break;
+      if (global_ns() - t0 > P.timeout_ns) {
+        *abort_flag = 1;
+        atomicOr(P.status, SV_FLAG_TIMEOUT);
+        break;
+      }
+      __nanosleep(200);
+    }
+  }
+  *out = code;
+  return code != 0;
+}
+
+// ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int kDtype>
@@ -682,68 +709,119 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
     float cached_c = 1.f;
     bool ok = true;
     const int K = P.K;
-    // Static items first (every first target row and every draft row,
-    // position-major), then the queued items (target rows the decisions
-    // wait for, and the draws' sample items): measured faster than letting
-    // queued items go first, as the static rows stream without interleaving
-    // and the chains then advance on a machine that is no longer saturated.
-    // Queued items are claimed with one atomicAdd each (a unique slot, no
-    // retries) and waited on (bounded) until published.
+    // Order of the claims.  Early exit: a target row some walk queued (its
+    // chain of decisions waits on it), else a static item (every first
+    // target row, then every draft row, position-major), else a sample item
+    // of a draw.  Each queue is claimed one slot at a time with atomicAdd
+    // (a unique slot, no contention on retries); a claimed slot stays
+    // pending until its entry is published and the producer looks at it
+    // between items, so it never waits for work that only other producers'
+    // rows could publish, and every published entry is staged by the
+    // producer holding its slot.  Without early exit: the static items, then
+    // the sample items in order (each is published by the scan of rows
+    // already staged).
     bool static_left = true, dyn_left = P.fused != 0;
+    uint64_t idle_t0 = 0;
+    int tq_pend = -1, dq_pend = -1;
+    bool tq_left = P.lazy != 0, dq_left = P.lazy != 0;
+    uint32_t backoff = 0;
     for (;;) {
-      int dyn = -1;
       int row_b = 0, row_chunk = 0, row_target = 0, row_pos = 0;
-      if (!static_left && dyn_left) {
-        const int c = (int)atomicAdd(P.dq_head, 1u);
-        if (c < P.ndyn) dyn = c;
-        else dyn_left = false;
-      }
-      int item;
-      if (dyn >= 0) {
-        item = P.nstatic + dyn;
-      } else {
-        if (!static_left) {
-          if (dyn_left) continue;
-          break;
+      int item = -1;
+      int code = 0;  // a sample item's 1-based code
+      if (P.lazy) {
+        if (tq_pend < 0 && tq_left) {
+          const int n = (int)atomicAdd(P.tq_head, 1u);
+          if (n < P.ntq) tq_pend = n;
+          else tq_left = false;
         }
-        item = (int)atomicAdd(P.ticket, 1u);
-        if (item >= P.nstatic) {
-          static_left = false;
-          continue;
-        }
-      }
-      if (item >= P.nstatic) {
-        // ---- a sample item: its slot is reserved; wait (bounded) for the entry
-        const int* slot = P.dq + (item - P.nstatic);
-        int code = ld_acquire_gpu(slot);
-        if (code == 0) {
-          const uint64_t t0 = global_ns();
-          while ((code = ld_acquire_gpu(slot)) == 0) {
-            if (*abort_flag) break;
-            if (global_ns() - t0 > P.timeout_ns) {
-              *abort_flag = 1;
-              atomicOr(P.status, SV_FLAG_TIMEOUT);
-              break;
-            }
-            __nanosleep(200);
-          }
-          if (code == 0) {
-            ok = false;
-            break;
-          }
-        }
-        if (code == kQueueNop) continue;
-        --code;
-        if (code >= P.B * P.sp) {
-          // a queued target row (early exit): (b K + i - 1) nch + chunk
-          const int r = code - P.B * P.sp;
+        int tcode = tq_pend >= 0 ? ld_acquire_gpu(P.tq + tq_pend) : 0;
+        if (tcode != 0) {
+          item = P.nstatic + tq_pend;
+          tq_pend = -1;
+          idle_t0 = 0;
+          backoff = 0;
+          if (tcode == kQueueNop) continue;
+          // a queued target row: (b K + i - 1) nch + chunk
+          const int r = tcode - 1;
           row_chunk = r % P.nch_dyn;
           const int q = r / P.nch_dyn;
           row_b = q / K;
           row_pos = q - row_b * K + 1;
           row_target = 1;
-          goto stage_row;
+        } else if (static_left && (item = (int)atomicAdd(P.ticket, 1u)) < P.nstatic) {
+          idle_t0 = 0;
+          // static items, position-major: group 0 = every first target row,
+          // group g >= 1 = every draft row g - 1 (measured: pairing each
+          // sequence's target and draft row 0 in one group is slower)
+          const int per_group = P.B * P.nch;
+          const int g = item / per_group;
+          const int rem = item - g * per_group;
+          row_b = rem / P.nch;
+          row_chunk = rem - row_b * P.nch;
+          row_target = g == 0;
+          row_pos = g == 0 ? 0 : g - 1;
+        } else {
+          static_left = false;
+          if (dq_pend < 0 && dq_left) {
+            const int n = (int)atomicAdd(P.dq_head, 1u);
+            if (n < P.ndyn) dq_pend = n;
+            else dq_left = false;
+          }
+          code = dq_pend >= 0 ? ld_acquire_gpu(P.dq + dq_pend) : 0;
+          if (code != 0) {
+            dq_pend = -1;
+            idle_t0 = 0;
+            backoff = 0;
+          } else {
+            if (!tq_left && !dq_left && tq_pend < 0 && dq_pend < 0) break;  // all work claimed and staged
+            // the pending slots are not published yet: look again shortly
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            const uint64_t now = global_ns();
+            if (idle_t0 == 0) {
+              idle_t0 = now;
+            } else if (now - idle_t0 > P.timeout_ns) {
+              *abort_flag = 1;
+              atomicOr(P.status, SV_FLAG_TIMEOUT);
+              ok = false;
+              break;
+            }
+            backoff = backoff ? min(2 * backoff, 1024u) : 64u;
+            __nanosleep(backoff);
+            continue;
+          }
         }
+      } else if (static_left) {
+        item = (int)atomicAdd(P.ticket, 1u);
+        if (item >= P.nstatic) {
+          static_left = false;
+          continue;
+        }
+        const int per_seq = P.nslot * P.nch;
+        row_b = item / per_seq;
+        const int rem = item - row_b * per_seq;
+        const int slot = rem / P.nch;
+        row_chunk = rem - slot * P.nch;
+        slot_kind(P.mode, K, slot, row_target, row_pos);
+      } else if (dyn_left) {
+        const int c = (int)atomicAdd(P.dq_head, 1u);
+        if (c >= P.ndyn) {
+          dyn_left = false;
+          continue;
+        }
+        if (!wait_entry(P, P.dq + c, abort_flag, &code)) {
+          ok = false;
+          break;
+        }
+      } else {
+        break;
+      }
+      if (code) {
+        // ---- a sample item (b, part) of a draw
+        --code;
         {
         const int b = code / P.sp, part = code - (code / P.sp) * P.sp;
         const SampleTask t = load_task_cg(P.tasks + b);
@@ -795,26 +873,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
         continue;
         }
       }
-      if (P.lazy) {
-        // static items, position-major: group 0 = every first target row,
-        // group g >= 1 = every draft row g - 1 (measured: pairing each
-        // sequence's target and draft row 0 in one group is slower)
-        const int per_group = P.B * P.nch;
-        const int g = item / per_group;
-        const int rem = item - g * per_group;
-        row_b = rem / P.nch;
-        row_chunk = rem - row_b * P.nch;
-        row_target = g == 0;
-        row_pos = g == 0 ? 0 : g - 1;
-      } else {
-        const int per_seq = P.nslot * P.nch;
-        row_b = item / per_seq;
-        const int rem = item - row_b * per_seq;
-        const int slot = rem / P.nch;
-        row_chunk = rem - slot * P.nch;
-        slot_kind(P.mode, K, slot, row_target, row_pos);
-      }
-    stage_row:
       const int b = row_b, chunk = row_chunk, is_target = row_target, pos = row_pos;
       if (b != cached_b) {
         cached_b = b;

@@ -125,9 +125,18 @@ struct RowPassParams {
   // early exit (fused verify modes): the static items are every sequence's
   // first target row and its draft rows, position-major (all t0, all d0,
   // all d1, ...); target row i + 1 of a sequence is queued when position i
-  // is accepted, so no target row past the first rejection is read.  Queue
-  // codes: 1 + b sp + part (sample items), 1 + B sp + (b K + i - 1) nch_dyn + chunk
-  // (target row i), kQueueNop (fillers that keep the queue's length fixed).
+  // is accepted, so no target row past the first rejection is read.  Queued
+  // target rows have a queue of their own, which producers serve before
+  // anything else: tq codes 1 + (b K + i - 1) nch_dyn + chunk (target row i)
+  // or kQueueNop (fillers for the rows a sequence never queued, which keep
+  // the queue's length at ntq = B K nch_dyn).  dq then holds only the sample
+  // items, 1 + b sp + part (ndyn = B sp).  A producer claims a slot of either
+  // queue only once it has been reserved, so no producer waits for work that
+  // only another producer's rows could publish.
+  int *tq;
+  uint32_t *tq_tail;
+  uint32_t *tq_head;
+  int ntq;
   int lazy;
   int ngroups;        // static groups: first target rows, then draft rows of each position
   int nch_dyn;        // chunks of a queued target row (shortens the chain of decisions)
@@ -142,7 +151,7 @@ constexpr int kMaxSampleParts = 16;
 
 struct WsLayout {
   size_t counters_off, counters_bytes;  // zeroed by every call
-  size_t ticket_off, fitacc_off, row_cnt_off, seq_cnt_off, smp_cnt_off, pos_cnt_off, dq_off;
+  size_t ticket_off, fitacc_off, row_cnt_off, seq_cnt_off, smp_cnt_off, pos_cnt_off, dq_off, tq_off;
   size_t stats_off, chunk_off, task_off, subsum_off;
   size_t total;
 };
@@ -155,8 +164,8 @@ inline WsLayout ws_layout(int B, int K, int V) {
   const size_t nsub = ((size_t)V + kSubChunk - 1) / kSubChunk;
   size_t off = 256;  // status word and spare header
   L.counters_off = off;
-  L.ticket_off = off;  // ticket, dq_tail, dq_head, scans_done
-  off += 16;
+  L.ticket_off = off;  // ticket, dq_tail, dq_head, scans_done, tq_tail, tq_head
+  off += 32;
   L.fitacc_off = off;  // [SV_MAX_K][6] 64-bit fixed point
   off += (size_t)SV_MAX_K * 6 * 8;
   L.row_cnt_off = off;
@@ -167,8 +176,10 @@ inline WsLayout ws_layout(int B, int K, int V) {
   off += (size_t)B * 4;
   L.pos_cnt_off = off;
   off += (size_t)B * (K + 1) * 4;
-  L.dq_off = off;  // last: a call clears only the entries it uses
-  off += (size_t)B * (kMaxSampleParts + (size_t)K * kMaxChunks) * 4;
+  L.dq_off = off;  // sample items [B][kMaxSampleParts]
+  off += (size_t)B * kMaxSampleParts * 4;
+  L.tq_off = off;  // last: a call clears only the entries it uses
+  off += (size_t)B * K * kMaxChunks * 4;
   off = align_up(off, 256);
   L.counters_bytes = off - L.counters_off;
   L.stats_off = off;
