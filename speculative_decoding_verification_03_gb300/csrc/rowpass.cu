@@ -359,10 +359,10 @@ __device__ void seq_event(const RowPassParams &P, int b, int k, int lane) {
 }
 
 // Target rows the walk queued when its accepted positions were 0..a-1 (see
-// rows_on_accept): rows 1..min(a + 1, k) with look-ahead, rows 1..a without.
+// rows_on_accept): rows 1..min(a + D, k) with a look-ahead of D rows.
 __device__ __forceinline__ int rows_queued(const RowPassParams &P, int a, int k) {
   if (a == 0) return 0;
-  return P.spec ? min(a + 1, k) : a;
+  return min(a + P.spec, k);
 }
 
 // The walk ended at position a (a < k: first rejection; a == k: all
@@ -464,20 +464,14 @@ __device__ __forceinline__ uint32_t pos_need(int i, int k) {
   return (i >= 1 ? 1u : 0u) + 1u + (i < k ? 1u : 0u);
 }
 // Target rows queued when position i is accepted, [*j0, *j1] (empty when
-// j1 < j0).  Each row is queued exactly once, by a fixed rule: with
-// look-ahead (P.spec) the acceptance of position 0 queues rows 1 and 2 and
-// that of position i >= 1 row i + 2 (row i + 1 came with position i - 1);
-// without it the acceptance of position i queues row i + 1.
+// j1 < j0).  Each row is queued exactly once, by a fixed rule with a
+// look-ahead of D = P.spec rows: the acceptance of position 0 queues rows
+// 1 .. 1 + D and that of position i >= 1 row i + 1 + D (rows up to i + D
+// came with earlier positions); rows past k are never queued.
 __device__ __forceinline__ void rows_on_accept(const RowPassParams &P, int i, int k, int *j0, int *j1) {
-  if (!P.spec) {
-    *j0 = *j1 = i + 1;
-  } else if (i == 0) {
-    *j0 = 1;
-    *j1 = min(2, k);
-  } else {
-    *j0 = *j1 = i + 2;
-    if (i + 2 > k) *j1 = i + 1;
-  }
+  const int last = i + 1 + P.spec;
+  *j0 = i == 0 ? 1 : last;
+  *j1 = min(last, k);
 }
 // lane 0: publish target rows j0..j1 of sequence b in the target-row queue
 // slots from base
@@ -724,6 +718,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
     uint64_t idle_t0 = 0;
     int tq_pend = -1, dq_pend = -1;
     bool tq_left = P.lazy != 0, dq_left = P.lazy != 0;
+    // a share of the CTAs serve the draws' sample items before static items
+    const bool draws_first = P.draw_every > 0 && (int)blockIdx.x % P.draw_every == 0;
     uint32_t backoff = 0;
     for (;;) {
       int row_b = 0, row_chunk = 0, row_target = 0, row_pos = 0;
@@ -749,32 +745,46 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
           row_b = q / K;
           row_pos = q - row_b * K + 1;
           row_target = 1;
-        } else if (static_left && (item = (int)atomicAdd(P.ticket, 1u)) < P.nstatic) {
-          idle_t0 = 0;
-          // static items, position-major: group 0 = every first target row,
-          // group g >= 1 = every draft row g - 1 (measured: pairing each
-          // sequence's target and draft row 0 in one group is slower)
-          const int per_group = P.B * P.nch;
-          const int g = item / per_group;
-          const int rem = item - g * per_group;
-          row_b = rem / P.nch;
-          row_chunk = rem - row_b * P.nch;
-          row_target = g == 0;
-          row_pos = g == 0 ? 0 : g - 1;
         } else {
-          static_left = false;
-          if (dq_pend < 0 && dq_left) {
-            const int n = (int)atomicAdd(P.dq_head, 1u);
-            if (n < P.ndyn) dq_pend = n;
-            else dq_left = false;
+          // then a static item and a published sample item of a draw, in
+          // this CTA's order (draws_first: a sample item first)
+          bool have = false;
+          for (int pass = 0; pass < 2 && !have; ++pass) {
+            if ((pass == 0) == draws_first) {
+              if (dq_pend < 0 && dq_left) {
+                const int n = (int)atomicAdd(P.dq_head, 1u);
+                if (n < P.ndyn) dq_pend = n;
+                else dq_left = false;
+              }
+              code = dq_pend >= 0 ? ld_acquire_gpu(P.dq + dq_pend) : 0;
+              if (code != 0) {
+                dq_pend = -1;
+                have = true;
+              }
+            } else if (static_left) {
+              item = (int)atomicAdd(P.ticket, 1u);
+              if (item < P.nstatic) {
+                // static items, position-major: group 0 = every first target
+                // row, group g >= 1 = every draft row g - 1 (measured: pairing
+                // each sequence's target and draft row 0 in one group is slower)
+                const int per_group = P.B * P.nch;
+                const int g = item / per_group;
+                const int rem = item - g * per_group;
+                row_b = rem / P.nch;
+                row_chunk = rem - row_b * P.nch;
+                row_target = g == 0;
+                row_pos = g == 0 ? 0 : g - 1;
+                have = true;
+              } else {
+                static_left = false;
+              }
+            }
           }
-          code = dq_pend >= 0 ? ld_acquire_gpu(P.dq + dq_pend) : 0;
-          if (code != 0) {
-            dq_pend = -1;
+          if (have) {
             idle_t0 = 0;
             backoff = 0;
           } else {
-            if (!tq_left && !dq_left && tq_pend < 0 && dq_pend < 0) break;  // all work claimed and staged
+            if (!static_left && !tq_left && !dq_left && tq_pend < 0 && dq_pend < 0) break;  // all claimed and staged
             // the pending slots are not published yet: look again shortly
             if (*abort_flag) {
               ok = false;

@@ -142,7 +142,8 @@ struct RowPassParams {
   int nch_dyn;        // chunks of a queued target row (shortens the chain of decisions)
   int chunk_elems_dyn;
   uint32_t *pos_cnt;  // [B][K+1]: events of position i (reached, target row, draft row)
-  int spec;           // look-ahead: queue target row i + 2 when position i >= 1 is accepted
+  int spec;           // look-ahead D: position i >= 1 accepted queues target row i + 1 + D
+  int draw_every;     // CTAs with blockIdx % draw_every == 0 take sample items before static items (0: none)
 };
 
 
