@@ -75,7 +75,9 @@ def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=
     Returns dict(tokens [B][N] (emitted, -1 after), accept_len [B], path [B][N-1]
     (accepted node indices, -1 after), flags [B], margin [B]: the smallest
     distance of a decision to its boundary -- |u - p(x)/q(x)| over the child
-    tests and the final draw's distance to its step edge (over R)).
+    tests and the final draw's distance to its step edge (over R);
+    acc_margin [B] and smp_margin [B]: the same over the child tests only and
+    over the final draw only; ndraws [B]: child tests that drew a uniform).
     seq_ids [B] or None: the request indices that key the uniforms."""
     t = np.asarray(target, dtype=np.float64)
     d = np.asarray(draft, dtype=np.float64)
@@ -89,6 +91,9 @@ def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=
     acc = np.zeros(B, np.int32)
     flags = np.zeros(B, np.int32)
     margin = np.full(B, np.inf)
+    acc_margin = np.full(B, np.inf)
+    smp_margin = np.full(B, np.inf)
+    ndraws = np.zeros(B, np.int32)
     sid = np.arange(B) if seq_ids is None else np.asarray(seq_ids, dtype=np.int64)
     for b in range(B):
         key = int(sid[b])
@@ -118,6 +123,8 @@ def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=
                     if 0 <= x < V:
                         ratio = np.inf if q[x] == 0 else p[x] / q[x]
                     margin[b] = min(margin[b], abs(u - ratio))
+                    acc_margin[b] = min(acc_margin[b], abs(u - ratio))
+                    ndraws[b] += 1
                     if u < ratio:
                         nxt = c
                         break
@@ -129,10 +136,12 @@ def verify_tree(target, draft, tokens, parents, temperature, seed: int, n_nodes=
                 if nxt is None:
                     out[b, depth], m = _draw(p, tree_uniform(seed, key, depth, 0, 1))
                     margin[b] = min(margin[b], m)
+                    smp_margin[b] = min(smp_margin[b], m)
                     break
             out[b, depth] = tok[b, nxt]
             path[b, depth] = nxt
             cur = nxt
             depth += 1
         acc[b] = depth
-    return dict(tokens=out, accept_len=acc, path=path, flags=flags, margin=margin)
+    return dict(tokens=out, accept_len=acc, path=path, flags=flags, margin=margin, acc_margin=acc_margin,
+                smp_margin=smp_margin, ndraws=ndraws)

@@ -227,10 +227,11 @@ def test_c3_fit_kernel_matches_oracle(c3_run):
     theta2 = torch.tensor(th, dtype=torch.float32, device=dev)
     st2 = binding.AVState(w.K, device=dev)
     st2.fit_step(theta2, torch.tensor(g["feature"], device=dev), torch.tensor(g["accept_len"], device=dev))
-    if np.array_equal(g["accept_len"], r["accept_len"]):
-        fit2 = oracle.AVFit(th)
-        fit2.step(r["feature"], r["accept_len"])
-        assert_rel(theta2.cpu().numpy(), fit2.theta, what="theta end to end")
+    # the oracle's refit on the GPU's own labels and features (they equal the
+    # oracle's except for sequences with a near-tie draw)
+    fit2 = oracle.AVFit(th)
+    fit2.step(g["feature"].astype(np.float64), g["accept_len"])
+    assert_rel(theta2.cpu().numpy(), fit2.theta, what="theta end to end")
 
 
 def test_fit_round_accumulation_on_gpu():
