@@ -495,6 +495,23 @@ void *sv_noalloc_status_holder(void);
  * ---------------------------------------------------------------------- */
 sv_status_t sv_set_launch_events(void *begin_event, void *end_event);
 
+/* ------------------------------------------------------------------------
+ * sv_set_wait_test -- a test hook for failure detection (the pages have no
+ * counterpart).  Applies to the later sv_verify, sv_verify_fit and
+ * sv_av_score calls made from the calling host thread until it is called
+ * again:
+ *   limit_ns  the limit of every device-side wait of their kernels, in ns
+ *             (0 = the default, 2 s);
+ *   withhold  nonzero: the kernels' producer warps stage no rows, so the
+ *             other warps' first waits can only end by running out (no copy
+ *             is ever in flight).  The call then writes no outputs and its
+ *             workspace status reports SV_FLAG_TIMEOUT (sv_status returns
+ *             SV_ERR_TIMEOUT) once limit_ns has passed; the device stays
+ *             usable, and the next call on the same workspace runs normally.
+ * For tests of the time-out path only.  Always returns SV_OK.
+ * ---------------------------------------------------------------------- */
+sv_status_t sv_set_wait_test(uint64_t limit_ns, int withhold);
+
 /* Static description of a status code; never NULL. */
 const char *sv_strerror(sv_status_t status);
 

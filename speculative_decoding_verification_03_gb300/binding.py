@@ -100,6 +100,8 @@ def lib():
             L.sv_philox.restype = I
             L.sv_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
             L.sv_status.restype = I
+            L.sv_set_wait_test.argtypes = [U64, I]
+            L.sv_set_wait_test.restype = I
             L.sv_set_launch_events.argtypes = [P, P]
             L.sv_set_launch_events.restype = I
             L.sv_post_verify.argtypes = [I, I, P, P, P, P, P, P, P, I, P, P, P]
@@ -418,6 +420,13 @@ def set_launch_events(begin=None, end=None):
     b = None if begin is None else ctypes.c_void_p(begin.cuda_event)
     e = None if end is None else ctypes.c_void_p(end.cuda_event)
     _check(lib().sv_set_launch_events(b, e), "sv_set_launch_events")
+
+
+def set_wait_test(limit_ns: int = 0, withhold: bool = False):
+    """sv_set_wait_test (failure-detection tests): the device waits' limit for
+    later calls from this thread (0 = default) and whether the producers
+    withhold all work so that the waits run out."""
+    _check(lib().sv_set_wait_test(ctypes.c_uint64(int(limit_ns)), 1 if withhold else 0), "sv_set_wait_test")
 
 
 def strerror(code: int) -> str:

@@ -83,6 +83,10 @@ void choose_chunks(int rows, int V, int sms, int &nch, int &chunk_elems) {
   nch = (V + ce - 1) / ce;
 }
 
+// Failure-detection test hook (sv_set_wait_test): per host thread.
+thread_local unsigned long long t_wait_limit_ns = 0;
+thread_local int t_withhold = 0;
+
 void fill_ws(RowPassParams &P, void *ws, const WsLayout &L) {
   unsigned char *w = static_cast<unsigned char *>(ws);
   P.status = reinterpret_cast<uint32_t *>(w);
@@ -92,7 +96,8 @@ void fill_ws(RowPassParams &P, void *ws, const WsLayout &L) {
   P.stats = reinterpret_cast<sv_row_stats_t *>(w + L.stats_off);
   P.chunk_part = reinterpret_cast<sv_row_stats_t *>(w + L.chunk_off);
   P.tasks = reinterpret_cast<SampleTask *>(w + L.task_off);
-  P.timeout_ns = kTimeoutNs;
+  P.timeout_ns = t_wait_limit_ns ? t_wait_limit_ns : kTimeoutNs;
+  P.withhold = t_withhold;
 }
 
 sv_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
@@ -433,6 +438,12 @@ sv_status_t sv_status(void *status_holder, void *stream, uint32_t *flags_out) {
   if (flags & SV_FLAG_TOKEN_RANGE) return SV_ERR_TOKEN_RANGE;
   if (flags & SV_FLAG_BAD_LEN) return SV_ERR_BAD_LEN;
   if (flags & SV_FLAG_BAD_TEMP) return SV_ERR_BAD_TEMP;
+  return SV_OK;
+}
+
+sv_status_t sv_set_wait_test(uint64_t limit_ns, int withhold) {
+  t_wait_limit_ns = limit_ns;
+  t_withhold = withhold != 0;
   return SV_OK;
 }
 

@@ -693,7 +693,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
-    if (lane != 0) return;
+    // (failure-detection tests: staging nothing leaves every consumer wait to
+    // run out; no copy is ever in flight)
+    if (lane != 0 || P.withhold) return;
     int s = 0;
     uint32_t phase = 0;
     uint32_t nfull[kStages];

@@ -37,11 +37,16 @@ __global__ void __launch_bounds__(kSampleThreads, kSampleCtasPerSm) sample_kerne
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const int gps = (P.nsub + kSampleUnroll - 1) / kSampleUnroll;
   const long long ngroups = (long long)P.B * gps;
+  // a row pass that gave up on a wait may have left tasks unwritten: draw
+  // nothing (the status word already reports the time-out)
+  if (__ldcg(P.status) & SV_FLAG_TIMEOUT) return;
   for (long long g = gwarp; g < ngroups; g += nwarps) {
     const int b = (int)(g / gps);
     const int jg = (int)(g - (long long)b * gps);
     const SampleTask t = P.tasks[b];
     if (t.kind == kTaskNone) continue;
+    if (!((t.kind == kTaskResidual && t.a >= 0 && t.a < P.K) || (t.kind == kTaskBonus && t.a >= 0 && t.a <= P.K)))
+      continue;  // never written by this launch's scans
     const RowPtrs R = row_ptrs(P, t, b, kEsz);
     const int j0 = jg * kSampleUnroll;
     group_sums<kDtype>(P, t, t.kind, R, j0, min(P.nsub, j0 + kSampleUnroll), lane, P.subsum + (size_t)b * P.nsub);

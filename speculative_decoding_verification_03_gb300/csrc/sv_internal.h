@@ -144,6 +144,7 @@ struct RowPassParams {
   uint32_t *pos_cnt;  // [B][K+1]: events of position i (reached, target row, draft row)
   int spec;           // look-ahead D: position i >= 1 accepted queues target row i + 1 + D
   int draw_every;     // CTAs with blockIdx % draw_every == 0 take sample items before static items (0: none)
+  int withhold;       // failure-detection tests: the producers stage nothing (sv_set_wait_test)
 };
 
 

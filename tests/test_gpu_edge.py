@@ -210,3 +210,50 @@ def test_zero_draft_probability_accepts(dtype):
     w = synth.Workload("qzero", B, K, V, dtype, t.contiguous(), d.to(dtype).contiguous(), toks, torch.ones(B))
     g_out, r = _check(w, 21)
     assert np.all(g_out["accept_len"] == K) and np.all(r["accept_len"] == K)
+
+
+@pytest.mark.parametrize("name", ["tiny", "c2"])
+def test_wait_timeout_is_reported_and_the_next_call_recovers(name):
+    """A device wait that runs out: with sv_set_wait_test's withhold, the
+    producer warps stage nothing, so every other warp's first wait can only
+    end by its limit (200 us here).  The call reports SV_ERR_TIMEOUT through
+    the workspace status, writes no output, and leaves the GPU usable: the
+    next call on the same workspace returns SV_OK and matches the oracle."""
+    dev = torch.device("cuda")
+    w = synth.WORKLOADS[name](seed=5)
+    g = w.to(dev)
+    B, K = w.B, w.K
+    ws = binding.workspace(B, K, w.V, dev)
+    th = torch.tensor(np.concatenate([[1.0], np.zeros(K)]), dtype=torch.float32, device=dev)
+    out = dict(tokens=torch.full((B, K + 1), -7, dtype=torch.int32, device=dev),
+               accept_len=torch.full((B,), -7, dtype=torch.int32, device=dev),
+               feature=torch.full((B, K), -7.0, device=dev), conf=torch.full((B, K), -7.0, device=dev))
+    binding.set_wait_test(limit_ns=200_000, withhold=True)
+    try:
+        binding.verify(g.target, g.draft, g.draft_tokens, g.temperature, 3, theta=th, want_feature=True, ws=ws,
+                       out=out)
+    finally:
+        binding.set_wait_test(0, False)
+    rc, flags = binding.status(ws)
+    assert rc == 6 and flags & binding.FLAG_TIMEOUT, (rc, flags)  # SV_ERR_TIMEOUT
+    for k in ("tokens", "accept_len", "feature", "conf"):
+        assert bool((out[k] == -7).all()), k  # nothing was written
+    res = gpu_verify(w, 3, theta=np.concatenate([[1.0], np.zeros(K)]), ws=ws)
+    assert res["rc"] == 0 and res["flags"] == 0, (res["rc"], res["flags"])
+    ref = oracle_verify(w, 3, theta=np.concatenate([[1.0], np.zeros(K)]))
+    compare(res, ref)
+    assert_rel(res["conf"], ref["conf"], what="conf after a time-out")
+
+
+def test_wait_limit_without_withholding_changes_nothing():
+    """The limit alone (a generous 5 s) leaves results and status unchanged."""
+    w = synth.c2(seed=9)
+    th = np.concatenate([[1.0], np.zeros(w.K)])
+    base = gpu_verify(w, 4, theta=th)
+    binding.set_wait_test(limit_ns=5_000_000_000, withhold=False)
+    try:
+        res = gpu_verify(w, 4, theta=th)
+    finally:
+        binding.set_wait_test(0, False)
+    assert res["rc"] == 0 and base["rc"] == 0
+    assert np.array_equal(res["tokens"], base["tokens"]) and np.array_equal(res["accept_len"], base["accept_len"])
