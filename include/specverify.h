@@ -462,7 +462,8 @@ sv_status_t sv_status(void *status_holder, void *stream, uint32_t *flags_out);
  *    (sv_workspace_bytes(B, K, V) > SV_NOALLOC_SCRATCH_BYTES) are rejected
  *    with SV_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on a device, with that device current, looks up the
- *    array's device address (once per device); make that first call before
+ *    array's device address (once per device and CUDA context: again after
+ *    a device reset has replaced the context); make that first call before
  *    any stream capture.
  *  - All calls share the one array, and the array keeps the last call's
  *    contents (each call clears what must start at zero).  Calls that
@@ -481,7 +482,7 @@ sv_status_t sv_verify_noalloc(int B, int K, int V, sv_dtype_t dtype,
                               float *out_feature, float *out_conf, void *stream);
 
 /* Device address of the scratch array's status word on the current device
- * (NULL before the first sv_verify_noalloc call there, or on error). */
+ * and context (looked up as by sv_verify_noalloc; NULL on error). */
 void *sv_noalloc_status_holder(void);
 
 /* ------------------------------------------------------------------------

@@ -465,19 +465,61 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRA
 
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[64];
+unsigned long long g_noalloc_ctx[64];
+
+// A process-unique id of the current CUDA context (0 if it cannot be read),
+// from the driver's cuCtxGetCurrent / cuCtxGetId, looked up through the
+// runtime so that the library does not link the driver library.  A device
+// reset replaces the context, and with it the scratch array's address.
+unsigned long long current_context_id() {
+  using GetCurrent = int (*)(void **);
+  using GetId = int (*)(void *, unsigned long long *);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+    looked_up = true;
+  }
+  void *ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == 0 && ctx && get_id(ctx, &id) == 0) return id;
+  return 0;
+}
+
+// The device address of the scratch array in the current context: looked up
+// once per device and context (cudaGetSymbolAddress), again after a device
+// reset created a new context, and on every call if the context's id cannot
+// be read.  The caller holds g_noalloc_mu.
+sv_status_t noalloc_scratch_locked(int dev, void **out) {
+  const unsigned long long ctx = current_context_id();
+  if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+      g_noalloc_ptr[dev] = nullptr;
+      return SV_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = ptr;
+    g_noalloc_ctx[dev] = ctx;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SV_OK;
+}
 
 sv_status_t noalloc_scratch(void **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
   if (dev < 0 || dev >= 64) return SV_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SV_ERR_CUDA;
-    g_noalloc_ptr[dev] = ptr;
-  }
-  *out = g_noalloc_ptr[dev];
-  return SV_OK;
+  return noalloc_scratch_locked(dev, out);
 }
 
 }  // namespace
@@ -500,10 +542,8 @@ sv_status_t sv_verify_noalloc(int B, int K, int V, sv_dtype_t dtype, const void 
 }
 
 void *sv_noalloc_status_holder(void) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  return g_noalloc_ptr[dev];
+  void *ptr = nullptr;
+  return noalloc_scratch(&ptr) == SV_OK ? ptr : nullptr;
 }
 
 const char *sv_strerror(sv_status_t s) {

@@ -257,3 +257,32 @@ def test_wait_limit_without_withholding_changes_nothing():
         binding.set_wait_test(0, False)
     assert res["rc"] == 0 and base["rc"] == 0
     assert np.array_equal(res["tokens"], base["tokens"]) and np.array_equal(res["accept_len"], base["accept_len"])
+
+
+@pytest.fixture(scope="module")
+def max_vocab_workload():
+    return synth.tiny(seed=31, B=2, K=2, V=1 << 24)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_maximum_vocabulary(dtype, max_vocab_workload):
+    """V = 2^24 (SV_MAX_V), B = 2, K = 2: the largest rows the library
+    accepts (16 split chunks per static row, a queued target row of 2^24
+    elements on one SM, 16 draw parts of 4096 sub-chunks).  At this V a
+    draw's CDF steps are about R / V wide, so nearly every draw lies within
+    1e-5 R of a step edge (a sampling near-tie); those are counted and must
+    still agree with the oracle."""
+    import dataclasses
+    w = max_vocab_workload
+    if dtype == torch.bfloat16:
+        w = dataclasses.replace(w, target=w.target.to(dtype).contiguous(), draft=w.draft.to(dtype).contiguous(),
+                                dtype=dtype)
+    for seed in (0, 1):
+        th = np.array([1.0, 0.0, 0.0])
+        g = gpu_verify(w, seed, theta=th)
+        assert g["rc"] == 0 and g["flags"] == 0, (g["rc"], g["flags"])
+        r = oracle_verify(w, seed, theta=th)
+        t = compare(g, r)
+        print("V = 2^24", dtype, "seed", seed, t)
+        assert t.tie_mismatch == 0, t
+        assert_rel(g["conf"], r["conf"], what="conf")

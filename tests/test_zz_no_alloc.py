@@ -69,6 +69,23 @@ def test_noalloc_matches_sv_verify_twice(lib, name):
         assert_rel(feat, ref["feature"].cpu().numpy(), what="feature")
 
 
+def test_noalloc_smaller_call_after_a_larger_one(lib):
+    """The largest shape first, then the smallest, on the shared scratch: the
+    small call's counters and queue entries sit where the large call left
+    other values, so this shows that each call clears what its own layout
+    needs."""
+    dev = torch.device("cuda")
+    for name, seed in (("c3", 21), ("tiny", 22), ("c2", 23), ("tiny", 24)):
+        w = synth.WORKLOADS[name](seed=seed, device=dev)
+        theta = torch.tensor([0.52] + [0.4 - 0.1 * i for i in range(w.K)], dtype=torch.float32, device=dev)
+        tok, acc, feat, conf = _noalloc(lib, w, seed, theta)
+        ref = binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, seed, theta=theta,
+                             want_feature=True)
+        assert np.array_equal(tok, ref["tokens"].cpu().numpy()), name
+        assert np.array_equal(acc, ref["accept_len"].cpu().numpy()), name
+        assert_rel(conf, ref["conf"].cpu().numpy(), what="conf " + name)
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch(lib):
     B, K, V = 1024, 16, 1 << 22
     assert lib.sv_workspace_bytes(B, K, V) > (8 << 20)
