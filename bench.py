@@ -381,32 +381,72 @@ def run_e2e(args, w, theta0, dev, steps=None):
                 d2h_bytes_per_step=d2h, steps=steps, wall_s=time.perf_counter() - t)
 
 
-def cpu_baseline(args, budget_s=12.0, max_seqs=None):
-    """The oracle as it stands, single-threaded, on sequences of the same
-    workload until about budget_s seconds of CPU work."""
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
+def _oracle_rate(w, K, threads, budget_s, max_seqs=None):
+    """Verified rows per second of the oracle (verify + one refit step per
+    call) on copies of the workload's sequences until budget_s has passed."""
     import numpy as np
 
     import oracle
-    from speculative_decoding_verification_03_gb300 import synth
 
-    cfg = WORKLOADS[args.workload]
-    B, K, V = cfg["B"], cfg["K"], cfg["V"]
-    n = 4 if args.workload != "c4" else 2
-    w = getattr(synth, args.workload)(seed=0, B=max(n, 2), device="cpu")
     th = np.array([1.0] + [0.0] * K)
-    tgt, drf = synth.logits_np(w.target), synth.logits_np(w.draft)
+    tgt, drf = synth_logits(w.target), synth_logits(w.draft)
     toks, tau = w.draft_tokens.numpy(), w.temperature.numpy()
-    done_rows, done_seqs, t0 = 0, 0, time.perf_counter()
+    done_rows, done_seqs, calls, t0 = 0, 0, 0, time.perf_counter()
     while time.perf_counter() - t0 < budget_s and (max_seqs is None or done_seqs < max_seqs):
-        r = oracle.verify(tgt, drf, toks, tau, done_seqs, theta=th)
+        r = oracle.verify(tgt, drf, toks, tau, calls, theta=th, threads=threads)
         fit = oracle.AVFit(th)
         fit.step(r["feature"], r["accept_len"])
         done_rows += int(w.B * (K + 1))
         done_seqs += w.B
+        calls += 1
     dt = time.perf_counter() - t0
-    return dict(value=done_rows / dt, unit="rows/s", cores=1, kind="oracle",
-                sample="%d sequences of the %s workload (B=%d, K=%d, V=%d), oracle verify + refit, %.1f s"
-                % (done_seqs, args.workload, B, K, V, dt))
+    return done_rows / dt, done_seqs, dt
+
+
+def synth_logits(t):
+    from speculative_decoding_verification_03_gb300 import synth
+    return synth.logits_np(t)
+
+
+def cpu_baseline(args, budget_s=12.0, max_seqs=None):
+    """The oracle as it stands (fp64, plain C) on the host: on every core
+    (its sequences split over threads) and on one core, on sequences of the
+    same workload, each leg about half of budget_s seconds."""
+    from speculative_decoding_verification_03_gb300 import synth
+
+    cfg = WORKLOADS[args.workload]
+    B, K, V = cfg["B"], cfg["K"], cfg["V"]
+    cores = os.cpu_count() or 1
+    n1 = 4 if args.workload != "c4" else 2
+    w1 = getattr(synth, args.workload)(seed=0, B=max(n1, 2), device="cpu")
+    v1, s1, t1 = _oracle_rate(w1, K, 1, budget_s / 2, max_seqs)
+    wn = getattr(synth, args.workload)(seed=0, B=max(2 * cores, n1), device="cpu")
+    vn, sn, tn = _oracle_rate(wn, K, cores, budget_s / 2, max_seqs)
+    return dict(value=vn, unit="rows/s", cores=cores, kind="oracle", cpu_model=cpu_model(),
+                sample="%d sequences of the %s workload (B=%d, K=%d, V=%d) in calls of %d, oracle verify + refit, "
+                "sequences split over %d threads, %.1f s" % (sn, args.workload, B, K, V, wn.B, cores, tn),
+                single_core=dict(value=v1, cores=1,
+                                 sample="%d sequences in calls of %d, one thread, %.1f s" % (s1, w1.B, t1)))
 
 
 # --------------------------------------------------------------------------- reference arm
@@ -422,19 +462,24 @@ def run_reference(args):
     oracle.build()
     cfg = WORKLOADS[args.workload]
     B, K, V = cfg["B"], cfg["K"], cfg["V"]
-    # size each step's sample so that warm-up + steps take about two minutes
-    w = getattr(synth, args.workload)(seed=0, B=8, device="cpu")
+    cores = os.cpu_count() or 1
+    # size each step's sample (a multiple of the core count, at most B) so
+    # that warm-up + steps take about two minutes on every host core
+    pool = min(B, 4 * cores)
+    w = getattr(synth, args.workload)(seed=0, B=pool, device="cpu")
     tgt, drf = synth.logits_np(w.target), synth.logits_np(w.draft)
     toks, tau = w.draft_tokens.numpy(), w.temperature.numpy()
     th = np.array([1.0] + [0.0] * K)
     t = time.perf_counter()
-    oracle.verify(tgt[:1], drf[:1], toks[:1], tau[:1], 0, theta=th)
-    per_seq = time.perf_counter() - t
-    n = int(max(1, min(8, 120.0 / max(1, args.steps + args.warmup) / per_seq)))
+    oracle.verify(tgt[:cores], drf[:cores], toks[:cores], tau[:cores], 0, theta=th, threads=cores)
+    per_round = time.perf_counter() - t  # one sequence per core
+    rounds = int(max(1, min(pool // cores, 120.0 / max(1, args.steps + args.warmup) / per_round)))
+    n = min(pool, rounds * cores)
 
     def step(i):
-        sl = slice((i * n) % (8 - n + 1), (i * n) % (8 - n + 1) + n)
-        r = oracle.verify(tgt[sl], drf[sl], toks[sl], tau[sl], i, theta=th)
+        s0 = (i * n) % (pool - n + 1)
+        sl = slice(s0, s0 + n)
+        r = oracle.verify(tgt[sl], drf[sl], toks[sl], tau[sl], i, theta=th, threads=cores)
         fit = oracle.AVFit(th)
         fit.step(r["feature"], r["accept_len"])
 
@@ -445,13 +490,13 @@ def run_reference(args):
         step(i)
     dt = time.perf_counter() - t0
     value = n * (K + 1) * args.steps / dt
-    sample = "%d of %d sequences per step (%s workload, V=%d), oracle verify + refit, 1 thread" % (
-        n, B, args.workload, V)
+    sample = "%d of %d sequences per step (%s workload, V=%d), oracle verify + refit, sequences split over %d " \
+        "threads (%s)" % (n, B, args.workload, V, cores, cpu_model())
     res = dict(impl="reference", metric=METRIC, value=value, unit="rows/s", n_gpus=world, steps=args.steps,
                warmup=args.warmup, ms_per_step=dt / args.steps * 1e3, higher_is_better=True, scaling="weak",
                vs_baseline=None, dtype="f64", data="synthetic",
                config=dict(workload=args.workload + ": " + cfg["desc"], B=B, K=K, V=V, logits="bf16"),
-               cpu_baseline=dict(value=value, unit="rows/s", cores=1, kind="oracle", sample=sample),
+               cpu_baseline=dict(value=value, unit="rows/s", cores=cores, kind="oracle", sample=sample),
                e2e=dict(value=value, unit="rows/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(res), flush=True)
 

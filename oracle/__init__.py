@@ -36,7 +36,7 @@ FLAG_BAD_LEN = 8
 FLAG_BAD_TEMP = 16
 
 
-_CFLAGS = ["-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared"]
+_CFLAGS = ["-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp"]
 
 
 def build(force: bool = False) -> str:
@@ -82,6 +82,8 @@ def _bind(path: str):
     lib.orc_verify.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P,
                                ctypes.c_uint64, P, P, P, P, P, P, P, P]
     lib.orc_verify.restype = None
+    lib.orc_verify_threads.argtypes = [ctypes.c_int] + lib.orc_verify.argtypes
+    lib.orc_verify_threads.restype = None
     lib.orc_av_accumulate.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
     lib.orc_av_accumulate.restype = None
     lib.orc_av_solve_update.argtypes = [ctypes.c_int, P, P, P, ctypes.c_double, P, P]
@@ -182,7 +184,8 @@ def av_score(draft, temperature, theta, keep_threshold: float = 0.0):
 # --------------------------------------------------------------------------
 # Verification step
 # --------------------------------------------------------------------------
-def verify(target, draft, draft_tokens, temperature, seed: int, draft_len=None, theta=None, seq_ids=None):
+def verify(target, draft, draft_tokens, temperature, seed: int, draft_len=None, theta=None, seq_ids=None,
+           threads: int = 1):
     """One verification step.
 
     target [B][K+1][V], draft [B][K][V] (uint16 bf16 bits or float32),
@@ -192,6 +195,8 @@ def verify(target, draft, draft_tokens, temperature, seed: int, draft_len=None, 
     acc_margin [B] (smallest |u - ratio| over the acceptance draws),
     smp_margin [B] (distance of u R to the chosen CDF step's nearer edge, / R),
     margin [B] (the smaller of the two), ndraws [B], flags [B]).
+    threads > 1 splits the sequences over that many host threads
+    (orc_verify_threads); the results are the same.
     """
     t, code = _logits(target)
     d, code2 = _logits(draft)
@@ -207,10 +212,13 @@ def verify(target, draft, draft_tokens, temperature, seed: int, draft_len=None, 
     out = dict(tokens=np.zeros((B, K + 1), np.int32), accept_len=np.zeros(B, np.int32),
                feature=np.zeros((B, K), np.float64), conf=np.zeros((B, K), np.float64),
                margins=np.zeros((B, 2), np.float64), ndraws=np.zeros(B, np.int32), flags=np.zeros(B, np.int32))
-    _load().orc_verify(B, K, V, code, _ptr(t), _ptr(d), _ptr(dt), _ptr(dl), _ptr(sid), _ptr(tau),
-                       int(seed) & (2**64 - 1),
-                       _ptr(th), _ptr(out["tokens"]), _ptr(out["accept_len"]), _ptr(out["feature"]),
-                       _ptr(out["conf"]), _ptr(out["margins"]), _ptr(out["ndraws"]), _ptr(out["flags"]))
+    args = (B, K, V, code, _ptr(t), _ptr(d), _ptr(dt), _ptr(dl), _ptr(sid), _ptr(tau), int(seed) & (2**64 - 1),
+            _ptr(th), _ptr(out["tokens"]), _ptr(out["accept_len"]), _ptr(out["feature"]), _ptr(out["conf"]),
+            _ptr(out["margins"]), _ptr(out["ndraws"]), _ptr(out["flags"]))
+    if threads > 1:
+        _load().orc_verify_threads(int(threads), *args)
+    else:
+        _load().orc_verify(*args)
     out["acc_margin"] = out["margins"][:, 0].copy()
     out["smp_margin"] = out["margins"][:, 1].copy()
     out["margin"] = out["margins"].min(axis=1)

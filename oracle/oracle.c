@@ -377,6 +377,46 @@ void orc_verify(int B, int K, int V, int dtype,
 }
 
 /* ------------------------------------------------------------------------ */
+/* orc_verify over the B sequences split into contiguous blocks, one per     */
+/* thread (OpenMP when compiled with it; one after another otherwise).  Each */
+/* block is orc_verify itself, keyed by the sequences' global indices (or    */
+/* seq_ids), so the results equal one orc_verify call over all B: the        */
+/* sequences of a step are independent.  Used to time the oracle on every    */
+/* host core; the arithmetic is orc_verify's.                                */
+/* ------------------------------------------------------------------------ */
+void orc_verify_threads(int nthreads, int B, int K, int V, int dtype,
+                        const void *target, const void *draft, const int32_t *draft_tokens,
+                        const int32_t *draft_len, const int32_t *seq_ids, const float *temperature,
+                        uint64_t seed, const double *theta,
+                        int32_t *out_tokens, int32_t *out_accept_len,
+                        double *out_feature, double *out_conf,
+                        double *out_margin, int32_t *out_ndraws, int32_t *out_flags)
+{
+    size_t rowb = (size_t)V * (dtype == 0 ? 2 : 4);
+    int nt = nthreads < 1 ? 1 : nthreads, t;
+    if (nt > B) nt = B > 0 ? B : 1;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nt) schedule(static, 1)
+#endif
+    for (t = 0; t < nt; t++) {
+        int b0 = (int)((long long)B * t / nt), b1 = (int)((long long)B * (t + 1) / nt), n = b1 - b0, i;
+        int32_t *sid;
+        if (n <= 0) continue;
+        sid = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+        for (i = 0; i < n; i++) sid[i] = seq_ids ? seq_ids[b0 + i] : (int32_t)(b0 + i);
+        orc_verify(n, K, V, dtype,
+                   (const char *)target + (size_t)b0 * (size_t)(K + 1) * rowb,
+                   (const char *)draft + (size_t)b0 * (size_t)K * rowb,
+                   draft_tokens + (size_t)b0 * K, draft_len ? draft_len + b0 : NULL, sid, temperature + b0,
+                   seed, theta, out_tokens + (size_t)b0 * (K + 1), out_accept_len + b0,
+                   out_feature ? out_feature + (size_t)b0 * K : NULL, out_conf ? out_conf + (size_t)b0 * K : NULL,
+                   out_margin ? out_margin + 2 * (size_t)b0 : NULL, out_ndraws ? out_ndraws + b0 : NULL,
+                   out_flags ? out_flags + b0 : NULL);
+        free(sid);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* [AV] "Fitting the coefficients".                                          */
 /* Labels: drafts up to and including the first rejection; accepted = 1,     */
 /* the rejected one = 0.  Accumulates the gradient g and Hessian H of the    */

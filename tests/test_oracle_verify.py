@@ -276,3 +276,20 @@ def test_zero_draft_probability_accepts():
         r = oracle.verify(tgt, drf, np.array([[1]], np.int32), np.ones(1, np.float32), seed)
         assert r["accept_len"][0] == 1 and r["tokens"][0, 0] == 1
         assert r["flags"][0] == 0
+
+
+def test_threaded_oracle_equals_single_thread():
+    """orc_verify_threads (the all-core timing of the oracle) splits the
+    sequences over threads; every output equals one single-threaded call,
+    with and without explicit sequence ids."""
+    w = synth.c2(seed=3, B=24, V=2003)
+    t, d = synth.logits_np(w.target), synth.logits_np(w.draft)
+    toks, tau = w.draft_tokens.numpy(), w.temperature.numpy()
+    th = np.concatenate([[0.7], 0.3 - 0.1 * np.arange(w.K)])
+    dl = np.arange(w.B, dtype=np.int32) % (w.K + 1)
+    for kw in (dict(), dict(seq_ids=np.arange(100, 124, dtype=np.int32), draft_len=dl)):
+        one = oracle.verify(t, d, toks, tau, 9, theta=th, **kw)
+        for n in (2, 5, 64):
+            many = oracle.verify(t, d, toks, tau, 9, theta=th, threads=n, **kw)
+            for k in one:
+                assert np.array_equal(one[k], many[k], equal_nan=True), (n, k)
