@@ -190,7 +190,7 @@ def run_gpu(args):
     import numpy as np
     import torch
 
-    from speculative_decoding_verification_03_gb300 import binding, synth
+    from speculative_decoding_verification_03_gb300 import binding, shard, synth
 
     world, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -227,17 +227,27 @@ def run_gpu(args):
     first_pass = w.bytes_first_pass()
     flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev) if first_pass <= L2_BYTES else None
 
+    # with several ranks every rank verifies its own block of sequences and
+    # the refit is the whole job's: each rank accumulates its labels
+    # (round_len 0), the 4K + 2 accumulator values are summed over the ranks
+    # (one all-reduce), and every rank solves for the same theta
+    sharded = world > 1
+    rl = 0 if sharded else 1
+
     def step(i, seed):
         out = outs[i]
+        seed = seed + (rank << 32)  # the ranks' sequences draw independent uniforms
         if score is not None:
             score["kept_len"] = kept[i]
             binding.av_score(w.draft, w.temperature, theta, keep_threshold=0.3, want_stats=True, ws=ws, out=score)
             binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, seed, draft_len=kept[i],
                            theta=theta, draft_stats=score["stats"], want_feature=True, ws=ws, out=out,
-                           av_state=state)
+                           av_state=state, round_len=rl)
         else:
             binding.verify(w.target, w.draft, w.draft_tokens, w.temperature, seed, theta=theta, want_feature=True,
-                           ws=ws, out=out, av_state=state)
+                           ws=ws, out=out, av_state=state, round_len=rl)
+        if sharded:
+            shard.end_round(state, theta)
 
     for i in range(args.warmup):
         step(i, 10**6 + i)
@@ -297,7 +307,7 @@ def run_gpu(args):
     # one launch of the row-pass kernel per step (verification, sampling and
     # the refit fused), plus the AV scoring row pass on the truncated canvas;
     # the workspace memset is a driver fill, not a kernel
-    launches_per_step = 1 + (1 if score is not None else 0)
+    launches_per_step = 1 + (1 if score is not None else 0) + (1 if sharded else 0)
 
     res = dict(metric=METRIC, value=value, unit="rows/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
                ms_per_step=elapsed_ms / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
@@ -336,7 +346,8 @@ def run_gpu(args):
                          l2=("inputs %.0f MB per step > 129 MB L2: no flush" % (first_pass / 1e6)) if flush is None
                          else ("inputs %.0f MB per step fit in the 129 MB L2: 256 MB written before every step; "
                                "steps timed by events around each step alone" % (first_pass / 1e6)),
-                         parallelism="replicas" if world > 1 else "single GPU")
+                         parallelism=("dp%d: a block of B sequences per GPU, one all-reduce of the AV refit "
+                                      "accumulators (4K + 2 fp64) per step" % world) if world > 1 else "single GPU")
     if rank == 0 and world == 1 and not args.no_e2e:
         res["e2e"] = run_e2e(args, w, theta0, dev)
     if rank == 0 and world == 1 and not args.no_cpu:
