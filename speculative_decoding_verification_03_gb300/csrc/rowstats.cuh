@@ -171,6 +171,11 @@ struct Elems<SV_BF16> {
     const uint32_t m = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
     return fmaxf(bf16lo(m), bf16hi(m));
   }
+  // a vector's maximum kept packed (as a bf16 pair), and its value
+  using PM = uint32_t;
+  __device__ __forceinline__ static PM pmax(const uint4 &v) { return bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w)); }
+  __device__ __forceinline__ static PM pmax2(PM a, PM b) { return bf16x2_max(a, b); }
+  __device__ __forceinline__ static float pval(PM m) { return fmaxf(bf16lo(m), bf16hi(m)); }
   // element `local` of the staged data := -inf
   __device__ __forceinline__ static void kill_smem(uint4 *ring, int local) {
     reinterpret_cast<unsigned short *>(ring)[local] = (unsigned short)0xff80u;
@@ -206,6 +211,10 @@ struct Elems<SV_FP32> {
   __device__ __forceinline__ static float vmax1(const uint4 &v) {
     return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
   }
+  using PM = float;
+  __device__ __forceinline__ static PM pmax(const uint4 &v) { return vmax1(v); }
+  __device__ __forceinline__ static PM pmax2(PM a, PM b) { return fmaxf(a, b); }
+  __device__ __forceinline__ static float pval(PM m) { return m; }
   __device__ __forceinline__ static void kill_smem(uint4 *ring, int local) {
     reinterpret_cast<uint32_t *>(ring)[local] = kNegInfF32;
   }
@@ -248,6 +257,33 @@ __device__ __forceinline__ void stage_rise(WarpState &s, uint4 *ring, int nvec, 
   state_rise(s, wm, gidx, c, lane);
 }
 
+// The same raise on a full stage, with the per-vector maxima of the first
+// pass (pm, in registers) instead of re-reading the stage: only the vector
+// holding the first copy of wm is read again.
+template <int kDtype>
+__device__ __forceinline__ void stage_rise_full(WarpState &s, uint4 *ring, int tid, int lane, int e0, float c, float wm,
+                                                const typename Elems<kDtype>::PM (&pm)[kVecPerThread]) {
+  using E = Elems<kDtype>;
+  int jv = -1;
+#pragma unroll
+  for (int j = kVecPerThread - 1; j >= 0; --j)
+    if (E::pval(pm[j]) == wm) jv = j;
+  int cand = INT_MAX;
+  if (jv >= 0) {
+    const int vi = tid + jv * kConsumers;
+    const uint4 v = ring[vi];
+    int k0 = E::kPerVec - 1;
+#pragma unroll
+    for (int k = E::kPerVec - 2; k >= 0; --k)
+      if (E::get(v, k) == wm) k0 = k;
+    cand = e0 + vi * E::kPerVec + k0;
+  }
+  const int gidx = warp_min_i(cand);
+  if (cand == gidx) E::kill_smem(ring, gidx - e0);
+  __syncwarp();
+  state_rise(s, wm, gidx, c, lane);
+}
+
 // exp2 terms of one 16-byte vector in packed pairs: fma2 for the arguments,
 // two MUFU ex2, add2 into four pair accumulators.
 template <int kDtype>
@@ -273,21 +309,26 @@ __device__ __forceinline__ void consume_stage(WarpState &s, uint4 *ring, int nve
   using E = Elems<kDtype>;
   const uint4 *base = ring + tid;
   const bool full = nvec == kVecPerStage;
-  float lm;
   if (full) {
-    uint4 w[kVecPerThread];
+    // per-vector maxima kept for a raise (about half of a row's stages raise
+    // some warp's running max)
+    typename E::PM pm[kVecPerThread];
 #pragma unroll
-    for (int j = 0; j < kVecPerThread; ++j) w[j] = base[j * kConsumers];
-    lm = E::vmax(w);
+    for (int j = 0; j < kVecPerThread; ++j) pm[j] = E::pmax(base[j * kConsumers]);
+    typename E::PM m = pm[0];
+#pragma unroll
+    for (int j = 1; j < kVecPerThread; ++j) m = E::pmax2(m, pm[j]);
+    const float wm = warp_max(E::pval(m));
+    if (wm > s.M) stage_rise_full<kDtype>(s, ring, tid, lane, e0, c, wm, pm);  // warp-uniform
   } else {
-    lm = -INFINITY;
+    float lm = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kVecPerThread; ++j)
       if (tid + j * kConsumers < nvec) lm = fmaxf(lm, E::vmax1(base[j * kConsumers]));
+    const float wm = warp_max(lm);
+    // the per-vector maxima are recomputed only when the warp max rises
+    if (wm > s.M) stage_rise<kDtype>(s, ring, nvec, tid, lane, e0, c, wm);  // warp-uniform
   }
-  const float wm = warp_max(lm);
-  // the per-vector maxima are recomputed only when the warp max rises (rare)
-  if (wm > s.M) stage_rise<kDtype>(s, ring, nvec, tid, lane, e0, c, wm);  // warp-uniform
   const float2 cc = make_float2(c, c), nb = make_float2(s.nbh, s.nbh);
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   if (full) {
