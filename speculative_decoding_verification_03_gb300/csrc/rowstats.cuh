@@ -228,40 +228,15 @@ struct Elems<SV_FP32> {
   }
 };
 
-// The running-max raise.  vm[j] is the max of this lane's vector j (pass 1);
-// the lane's first element equal to wm lies in its first vector with
-// vm[j] == wm.  The lane owning the first copy of wm overwrites it with -inf
-// in shared memory (the stage is this warp's until released, and only this
-// lane reads that vector), then the lane sums are rescaled.
+// The running-max raise.  pm[j] is the max of this lane's vector j from the
+// first pass (kept in registers; -inf past the stage's end), so the lane's
+// first element equal to wm lies in its first vector with pm[j] == wm, and
+// only that vector is read again.  The lane owning the first copy of wm
+// overwrites it with -inf in shared memory (the stage is this warp's until
+// released, and only this lane reads that vector), then the lane sums are
+// rescaled.
 template <int kDtype>
-__device__ __forceinline__ void stage_rise(WarpState &s, uint4 *ring, int nvec, int tid, int lane, int e0, float c,
-                                           float wm) {
-  using E = Elems<kDtype>;
-  int jv = -1;
-#pragma unroll
-  for (int j = kVecPerThread - 1; j >= 0; --j)
-    if (tid + j * kConsumers < nvec && E::vmax1(ring[tid + j * kConsumers]) == wm) jv = j;
-  int cand = INT_MAX;
-  if (jv >= 0) {
-    const int vi = tid + jv * kConsumers;
-    const uint4 v = ring[vi];
-    int k0 = E::kPerVec - 1;
-#pragma unroll
-    for (int k = E::kPerVec - 2; k >= 0; --k)
-      if (E::get(v, k) == wm) k0 = k;
-    cand = e0 + vi * E::kPerVec + k0;
-  }
-  const int gidx = warp_min_i(cand);
-  if (cand == gidx) E::kill_smem(ring, gidx - e0);
-  __syncwarp();
-  state_rise(s, wm, gidx, c, lane);
-}
-
-// The same raise on a full stage, with the per-vector maxima of the first
-// pass (pm, in registers) instead of re-reading the stage: only the vector
-// holding the first copy of wm is read again.
-template <int kDtype>
-__device__ __forceinline__ void stage_rise_full(WarpState &s, uint4 *ring, int tid, int lane, int e0, float c, float wm,
+__device__ __forceinline__ void stage_rise(WarpState &s, uint4 *ring, int tid, int lane, int e0, float c, float wm,
                                                 const typename Elems<kDtype>::PM (&pm)[kVecPerThread]) {
   using E = Elems<kDtype>;
   int jv = -1;
@@ -319,15 +294,17 @@ __device__ __forceinline__ void consume_stage(WarpState &s, uint4 *ring, int nve
 #pragma unroll
     for (int j = 1; j < kVecPerThread; ++j) m = E::pmax2(m, pm[j]);
     const float wm = warp_max(E::pval(m));
-    if (wm > s.M) stage_rise_full<kDtype>(s, ring, tid, lane, e0, c, wm, pm);  // warp-uniform
+    if (wm > s.M) stage_rise<kDtype>(s, ring, tid, lane, e0, c, wm, pm);  // warp-uniform
   } else {
-    float lm = -INFINITY;
+    // a row's last stage: vectors past nvec count as -inf
+    typename E::PM pm[kVecPerThread];
 #pragma unroll
-    for (int j = 0; j < kVecPerThread; ++j)
-      if (tid + j * kConsumers < nvec) lm = fmaxf(lm, E::vmax1(base[j * kConsumers]));
-    const float wm = warp_max(lm);
-    // the per-vector maxima are recomputed only when the warp max rises
-    if (wm > s.M) stage_rise<kDtype>(s, ring, nvec, tid, lane, e0, c, wm);  // warp-uniform
+    for (int j = 0; j < kVecPerThread; ++j) pm[j] = E::pmax(tid + j * kConsumers < nvec ? base[j * kConsumers] : E::neg_inf());
+    typename E::PM m = pm[0];
+#pragma unroll
+    for (int j = 1; j < kVecPerThread; ++j) m = E::pmax2(m, pm[j]);
+    const float wm = warp_max(E::pval(m));
+    if (wm > s.M) stage_rise<kDtype>(s, ring, tid, lane, e0, c, wm, pm);  // warp-uniform
   }
   const float2 cc = make_float2(c, c), nb = make_float2(s.nbh, s.nbh);
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
