@@ -241,17 +241,21 @@ sv_status_t verify_impl(int B, int K, int V, sv_dtype_t dtype, const void *targe
       P.tq = reinterpret_cast<int *>(w + L.tq_off);
       P.tq_tail = P.ticket + 4;
       P.tq_head = P.ticket + 5;
-      // Reading target row i + 2 one step ahead costs the rows of positions
-      // rejected at i + 1 and shortens each sequence's chain of decisions:
-      // measured faster while the streamed rows are under ~1 GB (the chains,
-      // not the bytes, bound the launch there: 64 x 5 x 32000 and
-      // 256 x 6 x 128256 bf16), slower above (1024 x 8 x 151936).
-      P.spec = (double)P.ngroups * B * V * esz < 1.0e9 ? 1 : 0;
-      // one CTA in eight serves the draws' sample items before static items,
-      // so the draws of sequences decided early do not all queue up behind
-      // the static rows (measured at B=256 K=5 V=128256: 1 in 8 145.1 ->
-      // 143.3 us, 1 in 4 145.3 us, 1 in 2 157.9 us; every CTA 154.8 us)
-      P.draw_every = 8;
+      // Reading target rows D positions ahead costs the rows of positions
+      // that are rejected before them and shortens each sequence's chain of
+      // decisions.  Measured (launch us, bf16): 64 x 5 x 32000 (37 MB of
+      // first-pass rows) D = 1 / 2 / 3: 62.3 / 57.4 / 56.5; 256 x 6 x 128256
+      // (722 MB) D = 0 / 1 / 2 / 3: 166 / 144.7 / 149.8 / 152.9; 1024 x 8 x
+      // 151936 (4.7 GB) D = 0 faster than D = 1.  The chains, not the bytes,
+      // bound the small launches.
+      const double first_pass = (double)B * (2 * K + 1) * V * esz;
+      P.spec = first_pass < 1.28e8 ? 3 : (first_pass < 1.0e9 ? 1 : 0);
+      // a share of the CTAs serve the draws' sample items before static
+      // items, so the draws of sequences decided early do not all queue up
+      // behind the static rows (measured at 256 x 6 x 128256: 1 in 8 145.1 ->
+      // 143.3 us, 1 in 4 145.3, 1 in 2 157.9, every CTA 154.8; at 1024 x 8 x
+      // 151936: 1 in 4 682 us against 689 us for 1 in 8)
+      P.draw_every = first_pass < 1.0e9 ? 8 : 4;
     } else {
       P.ndyn = B * sp;
     }
