@@ -580,7 +580,9 @@ def run_op(args):
         wt = torch.tensor([0.9 ** k for k in range(K)], dtype=torch.float32, device=dev)
         kl_out = torch.empty((B, K), dtype=torch.float32, device=dev)
         grad = torch.empty((B, K, V), dtype=torch.bfloat16, device=dev)
-        call = lambda i: binding.tts_signal(w.target, w.draft, w.temperature, wt, out_kl=kl_out, out_grad=grad)
+        tws = binding.tts_workspace(dev)
+        call = lambda i: binding.tts_signal(w.target, w.draft, w.temperature, wt, out_kl=kl_out, out_grad=grad,
+                                            workspace=tws)
         units, unit = B * K, "canvas positions/s"
         nbytes = B * K * V * 2 * 3 + B * K * 4  # both rows read once, the gradient written once
     elif op == "tree":
@@ -620,7 +622,7 @@ def run_op(args):
     value = units / (mean_ms / 1e3)
     peak, kind = _peak()
     achieved = nbytes / (mean_ms / 1e3) / 1e9
-    kernel = dict(budget="av_budget_kernel", post="post_verify_kernel", tts="tts_kernel", tree="tree_kernel")[op]
+    kernel = dict(budget="av_budget_kernel", post="post_verify_kernel", tts="tts_group_kernel", tree="tree_kernel")[op]
     res_line = dict(metric=unit.replace("/s", " per second") + " (" + op + ")", value=value, unit=unit, n_gpus=1,
                     steps=args.steps, warmup=args.warmup, ms_per_step=mean_ms, higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",

@@ -326,12 +326,23 @@ sv_status_t sv_av_budget(int B, int K, const float *conf, const int32_t *draft_l
  *   weights        device float [K]
  *   out_kl         device float [B][K]
  *   out_grad       device bf16 bits [B][K][V] or NULL (KL only)
- * Reads every row pair twice (the second time mostly from L2) and writes
- * the gradient once.  Returns after enqueueing.
+ *   workspace      device, >= sv_tts_workspace_bytes(), 256-byte aligned:
+ *                  the status word and the exchange between the CTAs that
+ *                  share a row pair; calls that share one workspace must be
+ *                  ordered (same stream, or events)
+ * With 16-byte aligned rows (V * element size a multiple of 16, and V a
+ * multiple of 8 when out_grad is given) every row pair is read from HBM
+ * once: a group of CTAs holds it in shared memory across both passes.
+ * Otherwise one CTA per pair reads it twice (the second time mostly from
+ * L2).  The gradient is written once.  A bounded wait that gives up sets
+ * SV_FLAG_TIMEOUT in the workspace's status word and the affected out_kl
+ * values are NaN.  Returns after enqueueing.
  * ---------------------------------------------------------------------- */
+size_t sv_tts_workspace_bytes(void);
 sv_status_t sv_tts_signal(int B, int K, int V, sv_dtype_t dtype, const void *target_logits,
                           const void *draft_logits, const float *temperature, const float *weights,
-                          float *out_kl, uint16_t *out_grad, void *stream);
+                          float *out_kl, uint16_t *out_grad, void *workspace, size_t workspace_bytes,
+                          void *stream);
 
 /* ------------------------------------------------------------------------
  * sv_verify_tree -- verification of a token tree (several draft branches per

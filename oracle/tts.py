@@ -45,7 +45,8 @@ def tts_signal(target, draft, temperature, weights, want_grad: bool = True):
             lq = _log_softmax(d[b, k] / tb)
             p = np.exp(lp)
             q = np.exp(lq)
-            terms = np.where(p > 0, p * (lp - lq), 0.0)
+            with np.errstate(invalid="ignore"):  # p = 0 where lp = -inf: the term is 0
+                terms = np.where(p > 0, p * (lp - lq), 0.0)
             kl[b, k] = w[k] * np.sum(terms)
             if want_grad:
                 grad[b, k] = w[k] * (q - p) / tb

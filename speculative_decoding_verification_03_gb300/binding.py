@@ -108,7 +108,9 @@ def lib():
             L.sv_post_verify.restype = I
             L.sv_av_budget.argtypes = [I, I, P, P, I, P, P, P, P, P]
             L.sv_av_budget.restype = I
-            L.sv_tts_signal.argtypes = [I, I, I, I, P, P, P, P, P, P, P]
+            L.sv_tts_workspace_bytes.argtypes = []
+            L.sv_tts_workspace_bytes.restype = SZ
+            L.sv_tts_signal.argtypes = [I, I, I, I, P, P, P, P, P, P, P, SZ, P]
             L.sv_tts_signal.restype = I
             L.sv_verify_tree.argtypes = [I, I, I, I, P, P, P, P, P, P, U64, P, P, P, P, P]
             L.sv_verify_tree.restype = I
@@ -352,9 +354,16 @@ def av_budget(conf, n_req: int, draft_cost, verify_cost, draft_len=None, out_bud
     return out_budget, out_kept_len
 
 
+def tts_workspace(device=None):
+    """A workspace for sv_tts_signal (sv_tts_workspace_bytes() bytes)."""
+    return torch.empty(int(lib().sv_tts_workspace_bytes()), dtype=torch.uint8,
+                       device=device if device is not None else "cuda")
+
+
 def tts_signal(target, draft, temperature, weights, want_grad: bool = True, out_kl=None, out_grad=None,
-               stream=None):
-    """sv_tts_signal: returns (kl [B][K] float32, grad [B][K][V] bfloat16 or None)."""
+               workspace=None, stream=None):
+    """sv_tts_signal: returns (kl [B][K] float32, grad [B][K][V] bfloat16 or None).
+    `workspace` (tts_workspace()) is allocated per call when not given."""
     B, K, V = draft.shape
     code = _dtype_code(target)
     if _dtype_code(draft) != code or target.shape != (B, K + 1, V):
@@ -367,8 +376,12 @@ def tts_signal(target, draft, temperature, weights, want_grad: bool = True, out_
         out_kl = torch.empty((B, K), dtype=torch.float32, device=draft.device)
     if want_grad and out_grad is None:
         out_grad = torch.empty((B, K, V), dtype=torch.bfloat16, device=draft.device)
+    if workspace is None:
+        workspace = tts_workspace(draft.device)
+    _dev(workspace, "workspace", torch.uint8)
     rc = lib().sv_tts_signal(B, K, V, code, _ptr(target), _ptr(draft), _ptr(temperature), _ptr(weights),
-                             _ptr(out_kl), _ptr(out_grad) if want_grad else None, _stream(stream))
+                             _ptr(out_kl), _ptr(out_grad) if want_grad else None, _ptr(workspace),
+                             workspace.numel(), _stream(stream))
     _check(rc, "sv_tts_signal")
     return out_kl, (out_grad if want_grad else None)
 

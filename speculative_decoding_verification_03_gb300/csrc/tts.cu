@@ -11,6 +11,7 @@
 // p (e^-d - 1 + d) with d = ln p - ln q, a sum of non-negative terms taken
 // by a short series for small |d|, so it keeps its relative precision when
 // q is close to p.
+#include <atomic>
 #include <cfloat>
 #include <mutex>
 
@@ -20,7 +21,7 @@
 namespace sv {
 namespace {
 
-constexpr int kTtsThreads = 512;
+constexpr int kTtsThreads = 256;
 constexpr int kTtsWarps = kTtsThreads / 32;
 constexpr int kTtsUnroll = 4;
 
@@ -36,6 +37,11 @@ struct TtsParams {
 
 template <int kDtype>
 struct TtsElems;
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 template <>
 struct TtsElems<SV_BF16> {
   static constexpr int kPer = 8;
@@ -43,6 +49,22 @@ struct TtsElems<SV_BF16> {
     const uint32_t x = (k >> 1) == 0 ? w.x : (k >> 1) == 1 ? w.y : (k >> 1) == 2 ? w.z : w.w;
     return (k & 1) ? bf16hi(x) : bf16lo(x);
   }
+  // elements e, e + 1 (e even): both halves of one word
+  __device__ __forceinline__ static float2 pair(const uint4 &w, int e) {
+    const uint32_t x = (e >> 1) == 0 ? w.x : (e >> 1) == 1 ? w.y : (e >> 1) == 2 ? w.z : w.w;
+    return make_float2(bf16lo(x), bf16hi(x));
+  }
+  // vector maximum / running minimum on the packed pairs
+  __device__ __forceinline__ static float vmax(const uint4 &w) {
+    const uint32_t m = bf16x2_max(bf16x2_max(w.x, w.y), bf16x2_max(w.z, w.w));
+    return fmaxf(bf16lo(m), bf16hi(m));
+  }
+  using MinT = uint32_t;
+  __device__ __forceinline__ static MinT min_init() { return 0x7f807f80u; }  // (+inf, +inf)
+  __device__ __forceinline__ static MinT min_acc(MinT a, const uint4 &w) {
+    return bf16x2_min(a, bf16x2_min(bf16x2_min(w.x, w.y), bf16x2_min(w.z, w.w)));
+  }
+  __device__ __forceinline__ static float min_fin(MinT a) { return fminf(bf16lo(a), bf16hi(a)); }
   __device__ __forceinline__ static float scalar(const void *row, int v) {
     return __uint_as_float(((uint32_t)reinterpret_cast<const uint16_t *>(row)[v]) << 16);
   }
@@ -53,6 +75,20 @@ struct TtsElems<SV_FP32> {
   __device__ __forceinline__ static float get(const uint4 &w, int k) {
     return __uint_as_float(k == 0 ? w.x : k == 1 ? w.y : k == 2 ? w.z : w.w);
   }
+  __device__ __forceinline__ static float2 pair(const uint4 &w, int e) {
+    return e == 0 ? make_float2(__uint_as_float(w.x), __uint_as_float(w.y))
+                  : make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+  }
+  __device__ __forceinline__ static float vmax(const uint4 &w) {
+    return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+  }
+  using MinT = float;
+  __device__ __forceinline__ static MinT min_init() { return INFINITY; }
+  __device__ __forceinline__ static MinT min_acc(MinT a, const uint4 &w) {
+    return fminf(a, fminf(fminf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                          fminf(__uint_as_float(w.z), __uint_as_float(w.w))));
+  }
+  __device__ __forceinline__ static float min_fin(MinT a) { return a; }
   __device__ __forceinline__ static float scalar(const void *row, int v) {
     return reinterpret_cast<const float *>(row)[v];
   }
@@ -127,6 +163,48 @@ __device__ __forceinline__ void online_add_vec2(Online &o, const uint4 &x, float
     }
     o.s += acc.x + acc.y;
   }
+}
+
+// Lazy reference for the row-pass statistics held in shared memory: the
+// terms are 2^(z c + nbh) with nbh = -m c for a reference m that is raised
+// only when a vector's terms would pass 2^64, which keeps any row's sum far
+// inside the fp32 range.  The reference is a logit of the row, so terms far
+// below the maximum underflow no earlier than with a running maximum; almost
+// every vector costs its exponentials and one compare, and the vector's
+// maximum is taken only on a raise.  The state starts at nbh = +inf, so the
+// first vector holding a finite logit raises (its sum is NaN or +inf).
+__device__ __forceinline__ Online lazy_init() { return {-INFINITY, 0.f, INFINITY, 0.f}; }
+template <typename E>
+__device__ __forceinline__ float lazy_terms(const uint4 &x, float c, float nbh) {
+  const float2 cc = make_float2(c, c), nb = make_float2(nbh, nbh);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int e = 0; e < E::kPer; e += 2) {
+    float2 t = __ffma2_rn(E::pair(x, e), cc, nb);
+    t.x = ex2_approx(t.x);
+    t.y = ex2_approx(t.y);
+    acc = __fadd2_rn(acc, t);
+  }
+  return acc.x + acc.y;
+}
+// set the reference from a vector's maximum before its terms are added
+template <typename E>
+__device__ __forceinline__ void lazy_seed(Online &o, const uint4 &x, float c) {
+  const float vm = E::vmax(x);
+  if (vm > -INFINITY) online_raise(o, vm, c);
+}
+template <typename E>
+__device__ __forceinline__ void lazy_add_vec2(Online &o, const uint4 &x, float c) {
+  float v = lazy_terms<E>(x, c, o.nbh);
+  if (!(v <= 0x1p64f)) {
+    const float vm = E::vmax(x);
+    v = 0.f;
+    if (vm > -INFINITY) {
+      online_raise(o, vm, c);
+      v = lazy_terms<E>(x, c, o.nbh);
+    }
+  }
+  o.s += v;
 }
 
 // (m, S = sum of 2^((z - m) c)) pairs for the cross-lane merge
@@ -329,242 +407,527 @@ __global__ void __launch_bounds__(kTtsThreads, 1) tts_kernel(const TtsParams P) 
 }
 
 // ---------------------------------------------------------------------------
-// Cluster kernel: the CTAs of one cluster share a row pair, each holding a
+// Shared-memory kernels: a group of CTAs shares a row pair, each holding a
 // slice of both rows in shared memory, so the second pass reads shared
-// memory instead of re-reading the rows.  Each slice is loaded by TMA bulk
-// copies in kTtsChunks chunks with one mbarrier each; as soon as the second
-// pass has finished a chunk, the same chunk of the next pair is requested,
-// so loads overlap compute with a single buffer.  Slice statistics are
-// exchanged through distributed shared memory (one cluster barrier per
-// pair); the KL partials of pair i are summed by rank 0 after the next
-// pair's barrier.  Rows must be 16-byte aligned with V * esz a multiple of 16
-// (the host falls back to tts_kernel otherwise).
+// memory instead of re-reading the rows.  A slice is loaded by TMA bulk
+// copies in kTtsChunks chunks with one mbarrier each.  Rows must be 16-byte
+// aligned with V * esz a multiple of 16 (the host falls back to tts_kernel
+// otherwise).
 // ---------------------------------------------------------------------------
-constexpr int kTtsChunks = 4;
+constexpr int kTtsChunks = 2;
+constexpr unsigned long long kTtsWaitNs = 2000000000ull;
 
-struct ClusterSmem {
-  uint64_t full[kTtsChunks];
-  float4 stats[2];   // this CTA's slice statistics (m_t, S_t, m_d, S_d) of even / odd pairs
-  float4 klpart[2];  // this CTA's KL partial of pairs of even / odd order (x), abort mark (y)
-  MS wt[kTtsWarps], wd[kTtsWarps];
-  float wk[kTtsWarps];
-  int abort;
-  uint32_t status;  // timeout bit of a bounded wait (the pair's KL is then NaN)
+// one vector's gradient values -> bf16 (streaming store)
+template <int kPer>
+__device__ __forceinline__ void store_grad(uint16_t *grow, int j, const float *g) {
+  if (kPer == 8) {
+    uint4 o;
+    o.x = bf16x2_rn(g[0], g[1]);
+    o.y = bf16x2_rn(g[2], g[3]);
+    o.z = bf16x2_rn(g[4], g[5]);
+    o.w = bf16x2_rn(g[6], g[7]);
+    __stcs(reinterpret_cast<uint4 *>(grow) + j, o);
+  } else {
+    uint2 o;
+    o.x = bf16x2_rn(g[0], g[1]);
+    o.y = bf16x2_rn(g[2], g[3]);
+    __stcs(reinterpret_cast<uint2 *>(grow) + j, o);
+  }
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_cta(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v) : "memory");
+  return old;
+}
+
+// butterfly merge of the lanes' (m, S) pairs; the pairwise merge is
+// symmetric, so every lane ends with the same value
+__device__ __forceinline__ void warp_merge2(MS &mt, MS &md, float c) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const MS a = {__shfl_xor_sync(0xffffffffu, mt.m, o), __shfl_xor_sync(0xffffffffu, mt.S, o)};
+    const MS d = {__shfl_xor_sync(0xffffffffu, md.m, o), __shfl_xor_sync(0xffffffffu, md.S, o)};
+    mt = ms_merge(mt, a, c);
+    md = ms_merge(md, d, c);
+  }
+}
+// Pass 1 over the vectors [v0, v1) of a chunk that fall to this thread
+// (stride kThreads): lazy statistics of both rows and the running minimum of
+// the target logits.  `seed` takes the reference from the thread's first
+// vector, so that vector's terms are not computed twice.
+template <typename E, int kThreads>
+__device__ __forceinline__ void pass1_chunk(const uint4 *tv, const uint4 *dv, int v0, int v1, int tid, bool seed,
+                                            float c, Online &ot, Online &od, typename E::MinT &zmin) {
+  int j = v0 + tid;
+  if (seed && j < v1) {
+    lazy_seed<E>(ot, tv[j], c);
+    lazy_seed<E>(od, dv[j], c);
+  }
+  for (; j < v1; j += kThreads) {
+    const uint4 xt = tv[j], xd = dv[j];
+    zmin = E::min_acc(zmin, xt);
+    lazy_add_vec2<E>(ot, xt, c);
+    lazy_add_vec2<E>(od, xd, c);
+  }
+}
+
+// Per-pair constants of the second pass.
+struct Pass2Const {
+  float c, at, ad, wg;  // log2 e / tau; log2 p = z_t c + at, log2 q = z_d c + ad; w / tau
+  float atf;            // at + log2(w / tau) (fast path)
+  float invh, nK0;      // 1 / tau and -K0 (d = (z_t - z_d) / tau - K0)
+  bool fold;            // w / tau in [2^-20, 2^20]: the fast path may fold it into p
+};
+__device__ __forceinline__ Pass2Const pass2_constants(const MS &mt, const MS &md, float tau, float c, float w) {
+  const PairConst pc = pair_constants(mt, md, tau);
+  Pass2Const k;
+  k.c = c;
+  k.at = -fmaf(mt.m, c, log2f(mt.S));
+  k.ad = -fmaf(md.m, c, log2f(md.S));
+  k.wg = w * pc.invh;
+  k.fold = k.wg >= 0x1p-20f && k.wg <= 0x1p20f;
+  k.atf = k.fold ? k.at + log2f(k.wg) : k.at;
+  k.invh = pc.invh;
+  k.nK0 = -(pc.K0h + pc.K0l);
+  return k;
+}
+// Warp-uniform choice of the fast path: w / tau folds into p, and every
+// target logit of the warp's vectors gives p' = (w / tau) p >= 2^-100, so p'
+// never underflows and e^-d = q / p stays finite (at most 2^120).
+template <typename E>
+__device__ __forceinline__ bool pass2_fast_ok(const Pass2Const &k, typename E::MinT zmin) {
+  const bool ok_t = fmaf(E::min_fin(zmin), k.c, k.atf) >= -100.f;  // +inf (no vectors) passes, -inf / NaN fail
+  return k.fold && __all_sync(0xffffffffu, ok_t);
+}
+
+// Pass 2 over the thread's vectors of [v0, v1).  Per element, with
+// d = ln p - ln q: the KL term p (e^-d - 1 + d) (by its series for |d| < 1/4,
+// where the direct form cancels) and the gradient (w / tau) (q - p) =
+// (w / tau) p (e^-d - 1).  The fast path works with p' = (w / tau) p, so its
+// KL sum carries the factor w / tau; the general path also covers p = 0
+// (z_t = -inf or an underflow), where both terms tend to q.
+template <typename E, int kThreads, bool kFast>
+__device__ __forceinline__ void pass2_chunk(const uint4 *tv, const uint4 *dv, int v0, int v1, int tid,
+                                            const Pass2Const &k, float2 &acc2, uint16_t *grow) {
+  constexpr int kPer = E::kPer;
+  const float2 cc2 = make_float2(k.c, k.c), invh2 = make_float2(k.invh, k.invh);
+  const float2 nK0 = make_float2(k.nK0, k.nK0), neg1 = make_float2(-1.f, -1.f);
+  const float2 c120 = make_float2(-1.f / 120.f, -1.f / 120.f), c24 = make_float2(1.f / 24.f, 1.f / 24.f);
+  const float2 c6 = make_float2(-1.f / 6.f, -1.f / 6.f), half2 = make_float2(0.5f, 0.5f);
+  const float2 nlog2e = make_float2(-kLog2e, -kLog2e);
+  const float a = kFast ? k.atf : k.at;
+  const float2 at2 = make_float2(a, a), wg2 = make_float2(k.wg, k.wg);
+  for (int j = v0 + tid; j < v1; j += kThreads) {
+    const uint4 xt = tv[j], xd = dv[j];
+    float g[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) {
+      const float2 zt = E::pair(xt, e), zd = E::pair(xd, e);
+      float2 p = __ffma2_rn(zt, cc2, at2);
+      p.x = ex2_approx(p.x);
+      p.y = ex2_approx(p.y);
+      const float2 d = __ffma2_rn(__ffma2_rn(zd, neg1, zt), invh2, nK0);
+      float2 ex = __fmul2_rn(d, nlog2e);  // e^-d = q / p
+      ex.x = ex2_approx(ex.x);
+      ex.y = ex2_approx(ex.y);
+      float2 poly = __ffma2_rn(d, c120, c24);
+      poly = __ffma2_rn(d, poly, c6);
+      poly = __ffma2_rn(d, poly, half2);  // (e^-d - 1 + d) / d^2 to fifth order
+      if (kFast) {
+        const float2 tg = __ffma2_rn(p, ex, make_float2(-p.x, -p.y));  // (w / tau) (q - p)
+        const float2 t = __fmul2_rn(p, d);
+        const float2 tl = __fadd2_rn(t, tg);
+        const float2 ts = __fmul2_rn(t, __fmul2_rn(d, poly));
+        acc2 = __fadd2_rn(acc2, make_float2(fabsf(d.x) < 0.25f ? ts.x : tl.x, fabsf(d.y) < 0.25f ? ts.y : tl.y));
+        g[e] = tg.x;
+        g[e + 1] = tg.y;
+      } else {
+        const float2 phi_s = __fmul2_rn(__fmul2_rn(d, d), poly);
+        const float2 em1 = __fadd2_rn(ex, neg1);  // e^-d - 1
+        const float2 phl = __fadd2_rn(em1, d);
+        const float2 phi = make_float2(fabsf(d.x) < 0.25f ? phi_s.x : phl.x, fabsf(d.y) < 0.25f ? phi_s.y : phl.y);
+        float2 tkl = __fmul2_rn(p, phi), tg = __fmul2_rn(p, em1);
+        if (!(p.x > 0.f) || !(p.y > 0.f)) {  // p = 0: the limits of both terms are q
+          if (!(p.x > 0.f)) tkl.x = tg.x = ex2_approx(fmaf(zd.x, k.c, k.ad));
+          if (!(p.y > 0.f)) tkl.y = tg.y = ex2_approx(fmaf(zd.y, k.c, k.ad));
+        }
+        acc2 = __fadd2_rn(acc2, tkl);
+        const float2 gg = __fmul2_rn(wg2, tg);
+        g[e] = gg.x;
+        g[e + 1] = gg.y;
+      }
+    }
+    if (grow) store_grad<kPer>(grow, j, g);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Group kernel: G CTAs (one per SM, any G up to 32, no cluster) share a row
+// pair, each holding a slice of S elements of both rows; nb = 2 or 3 pair
+// slices stay resident per CTA.  The slice is copied in kTtsChunks chunks,
+// each owned by kGrpWarps / kTtsChunks compute warps, so a warp waits for
+// one copy and releases one chunk per pair.  Per pair i a compute thread
+// runs the statistics of pair i + 1 (left in shared memory), then the
+// second pass of pair i (its KL partial left in shared memory); a chunk
+// released by all its warps is refilled with pair i + nb.  A coordinator
+// warp merges the threads' statistics into the CTA's entry and publishes it
+// in the workspace; it gathers the group's G entries of a pair, merges them
+// in rank order and derives the row constants once for the CTA; it sums the
+// threads' KL partials, and on rank 0 sums the group's partials in rank
+// order into out_kl two pairs later.  No compute warp waits on another SM.
+// Every 64-bit word of the exchange holds a 32-bit value and a 32-bit tag
+// (the call's generation and the pair's use of the slot), and each word is
+// stored and loaded whole, so one relaxed load both tests and reads an
+// entry; words of an earlier call or an earlier use of the slot never
+// match.
+// ---------------------------------------------------------------------------
+constexpr int kGrpWarps = 16;                        // compute warps
+constexpr int kGrpCompute = kGrpWarps * 32;
+constexpr int kGrpThreads = kGrpCompute + 32;        // + the coordinator warp
+constexpr int kChunkWarps = kGrpWarps / kTtsChunks;  // warps that own a chunk
+constexpr int kChunkThreads = kChunkWarps * 32;
+constexpr int kGrpMaxNb = 3;
+constexpr int kGrpSlots = 4;                         // pairs whose exchange may be in flight
+constexpr int kTtsMaxGroup = 32;
+constexpr int kTtsMaxCtas = 1024;
+static_assert(kGrpWarps % kTtsChunks == 0, "whole warps per chunk");
+constexpr size_t kTtsWsHeader = 256;                 // status word and spare
+// workspace: header, then per slot and CTA the statistics entry (four tagged
+// words: m_t, S_t, m_d, S_d), then per slot and CTA the tagged KL partial
+constexpr size_t kTtsWsStat = kTtsWsHeader;
+constexpr size_t kTtsWsKl = kTtsWsStat + (size_t)kGrpSlots * kTtsMaxCtas * 32;
+constexpr size_t kTtsWsBytes = kTtsWsKl + (size_t)kGrpSlots * kTtsMaxCtas * 8;
+
+struct GroupArgs {
+  int G, S, nb;
+  uint32_t gen;         // call generation (tags)
+  unsigned char *ws;    // workspace (kTtsWsBytes)
 };
 
+struct GroupSmem {
+  uint64_t full[kGrpMaxNb][kTtsChunks];
+  uint64_t stat_bar[2];            // the compute threads' statistics of pairs of even / odd order
+  uint64_t kl_bar[2];              // their KL partials
+  uint64_t const_bar[kGrpSlots];   // a pair's constants are ready (coordinator)
+  uint32_t released[kGrpMaxNb][kTtsChunks];
+  uint32_t issued[kGrpMaxNb][kTtsChunks];
+  Pass2Const pc[kGrpSlots];
+  float scale[kGrpSlots];          // out_kl = scale * (sum of the partials)
+  int pc_ok[kGrpSlots];
+  int abort;                       // a wait timed out: no further copies, outputs of later pairs are NaN
+  float4 tstat[2][kGrpCompute];    // per thread (m_t, S_t, m_d, S_d)
+  float tkl[2][kGrpCompute];       // per thread KL partial
+};
+
+// tagged words: value bits low, tag high
+__device__ __forceinline__ unsigned long long tagged(float v, uint32_t tag) {
+  return ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v);
+}
+__device__ __forceinline__ float untag(unsigned long long w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ bool tag_is(unsigned long long w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+__device__ __forceinline__ void st_words2(unsigned long long *p, unsigned long long a, unsigned long long b) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void ld_words2(const unsigned long long *p, unsigned long long &a, unsigned long long &b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_word(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_word(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Waits of the group kernel poll a barrier between sleeps that double from
+// 32 ns up to max_ns, so a waiting warp leaves its scheduler's issue slots
+// to the warps that compute.  Both are bounded by kTtsWaitNs and set
+// SV_FLAG_TIMEOUT when they give up.
+// Chunk copies: also gives up as soon as another thread set the abort flag.
+__device__ __forceinline__ bool wait_copy(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          uint32_t *status, uint32_t max_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t ns = 32;; ns = ns < max_ns ? 2 * ns : max_ns) {
+    __nanosleep(ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kTtsWaitNs) {
+      *abort_flag = 1;
+      atomicOr(status, SV_FLAG_TIMEOUT);
+      return false;
+    }
+  }
+}
+// CTA-local barriers: every arrival on them happens even after an abort, so
+// they always complete; time-bounded only
+__device__ __forceinline__ bool mbar_wait_local(uint64_t *bar, uint32_t parity, uint32_t *status, uint32_t max_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t ns = 32;; ns = ns < max_ns ? 2 * ns : max_ns) {
+    __nanosleep(ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kTtsWaitNs) {
+      atomicOr(status, SV_FLAG_TIMEOUT);
+      return false;
+    }
+  }
+}
+// lanes < n read their record (nw = 4: a statistics entry, 1: a KL partial)
+// until every word carries `tag` (warp-uniform result, bounded; nanosleep
+// back-off between polls)
+template <int nw>
+__device__ __forceinline__ bool poll_records(const unsigned long long *rec, int n, int lane, uint32_t tag,
+                                             unsigned long long (&w)[4], uint32_t *status) {
+  auto load = [&]() {
+    if (lane >= n) return true;
+    if (nw == 4) {
+      ld_words2(rec + 4 * lane, w[0], w[1]);
+      ld_words2(rec + 4 * lane + 2, w[2], w[3]);
+      return tag_is(w[0], tag) && tag_is(w[1], tag) && tag_is(w[2], tag) && tag_is(w[3], tag);
+    }
+    w[0] = ld_word(rec + lane);
+    return tag_is(w[0], tag);
+  };
+  bool mine = load();
+  if (__all_sync(0xffffffffu, mine)) return true;
+  const uint64_t t0 = __shfl_sync(0xffffffffu, global_ns(), 0);
+  uint32_t ns = 32;
+  for (;;) {
+    __nanosleep(ns);
+    if (ns < 1024) ns <<= 1;
+    if (!mine) mine = load();
+    if (__all_sync(0xffffffffu, mine)) return true;
+    if (__shfl_sync(0xffffffffu, global_ns() - t0 > kTtsWaitNs ? 1 : 0, 0)) {
+      if (lane == 0) atomicOr(status, SV_FLAG_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 template <int kDtype>
-__global__ void __launch_bounds__(kTtsThreads, 1) tts_cluster_kernel(const TtsParams P, int S) {
+__global__ void __launch_bounds__(kGrpThreads, 1) tts_group_kernel(const TtsParams P, const GroupArgs A) {
   using E = TtsElems<kDtype>;
+  using MinT = typename E::MinT;
   constexpr int kEsz = kDtype == SV_BF16 ? 2 : 4;
   constexpr int kPer = E::kPer;
   extern __shared__ __align__(128) uint8_t tts_smem[];
-  ClusterSmem &C = *reinterpret_cast<ClusterSmem *>(tts_smem);
-  uint8_t *buf = tts_smem + ((sizeof(ClusterSmem) + 127) / 128) * 128;
-  const size_t slice_bytes = (size_t)S * kEsz;  // target slice, then draft slice
+  GroupSmem &R = *reinterpret_cast<GroupSmem *>(tts_smem);
+  uint8_t *ring = tts_smem + ((sizeof(GroupSmem) + 127) / 128) * 128;
+  const size_t slice_bytes = (size_t)A.S * kEsz;  // per buffer: target slice, then draft slice
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int V = P.V, K = P.K;
-  const uint32_t rank = cluster_ctarank();
-  const int cs = (int)(gridDim.x / ncluster_x());
-  const int cid = (int)cluster_id_x(), ncl = (int)ncluster_x();
+  const int V = P.V, K = P.K, G = A.G, nb = A.nb;
+  const int cta = (int)blockIdx.x, grp = cta / G, rank = cta - grp * G;
+  const int ngroups = (int)gridDim.x / G;
   const int npairs = P.B * K;
-  const int e0 = (int)rank * S, e1 = min(V, e0 + S);
+  const int npairs_g = grp < npairs ? (npairs - grp + ngroups - 1) / ngroups : 0;  // pairs of this group
+  const int e0 = rank * A.S, e1 = min(V, e0 + A.S);
   const int nel = max(0, e1 - e0);
-  const int nvec = nel / kPer;                                 // 16-byte vectors of the slice
-  const int cvec = (nvec + kTtsChunks - 1) / kTtsChunks;       // vectors per chunk
+  const int nvec = nel / kPer;
+  const int cvec = (nvec + kTtsChunks - 1) / kTtsChunks;
+  uint32_t *status = reinterpret_cast<uint32_t *>(A.ws);
+  unsigned long long *g_stat = reinterpret_cast<unsigned long long *>(A.ws + kTtsWsStat);
+  unsigned long long *g_kl = reinterpret_cast<unsigned long long *>(A.ws + kTtsWsKl);
+  // a slot's previous content is from the same call four pairs earlier (other
+  // phase bit) or from an earlier call (other generation)
+  auto tag_of = [&](int it) { return (A.gen << 1) | (uint32_t)((it >> 2) & 1); };
 
   if (tid == 0) {
-    for (int ch = 0; ch < kTtsChunks; ++ch) mbar_init(&C.full[ch], 1);
-    C.abort = 0;
-    C.status = 0;
-    C.klpart[0] = C.klpart[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int bi = 0; bi < kGrpMaxNb; ++bi)
+      for (int ch = 0; ch < kTtsChunks; ++ch) {
+        mbar_init(&R.full[bi][ch], 1);
+        R.released[bi][ch] = 0;
+        R.issued[bi][ch] = 0;
+      }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&R.stat_bar[s], kGrpCompute);
+      mbar_init(&R.kl_bar[s], kGrpCompute);
+    }
+    for (int s = 0; s < kGrpSlots; ++s) mbar_init(&R.const_bar[s], 1);
+    R.abort = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
-  // thread 0: request chunk ch of the it-th pair of this cluster
+  // request chunk ch of the it-th pair of this group into buffer it % nb
   auto issue = [&](int it, int ch) {
-    const int pair = cid + it * ncl;
-    if (pair >= npairs) return;
+    if (it >= npairs_g) return;
+    const int pair = grp + it * ngroups;
+    const int bi = it % nb;
     const int b = pair / K, k = pair - b * K;
     const int v0 = min(nvec, ch * cvec), v1 = min(nvec, v0 + cvec);
     const uint32_t bytes = (uint32_t)(v1 - v0) * 16u;
-    mbar_arrive_expect_tx(&C.full[ch], 2 * bytes);
+    uint8_t *buf = ring + (size_t)bi * 2 * slice_bytes;
+    R.issued[bi][ch] += 1;
+    mbar_arrive_expect_tx(&R.full[bi][ch], 2 * bytes);
     if (bytes) {
       const char *trow = reinterpret_cast<const char *>(P.target) + ((size_t)b * (K + 1) + k) * (size_t)V * kEsz;
       const char *drow = reinterpret_cast<const char *>(P.draft) + ((size_t)b * K + k) * (size_t)V * kEsz;
       const size_t off = (size_t)e0 * kEsz + (size_t)v0 * 16;
-      bulk_g2s(buf + (size_t)v0 * 16, trow + off, bytes, &C.full[ch]);
-      bulk_g2s(buf + slice_bytes + (size_t)v0 * 16, drow + off, bytes, &C.full[ch]);
+      bulk_g2s(buf + (size_t)v0 * 16, trow + off, bytes, &R.full[bi][ch]);
+      bulk_g2s(buf + slice_bytes + (size_t)v0 * 16, drow + off, bytes, &R.full[bi][ch]);
     }
   };
   if (tid == 0)
-    for (int ch = 0; ch < kTtsChunks; ++ch) issue(0, ch);
+    for (int i = 0; i < nb; ++i)
+      for (int ch = 0; ch < kTtsChunks; ++ch) issue(i, ch);
 
-  volatile int *abort_flag = &C.abort;
-  const uint4 *tv = reinterpret_cast<const uint4 *>(buf);
-  const uint4 *dv = reinterpret_cast<const uint4 *>(buf + slice_bytes);
-  int it = 0, prev_b = -1, prev_k = 0;
-  float prev_w = 0.f;
-  for (int pair = cid; pair < npairs; pair += ncl, ++it) {
-    const int b = pair / K, k = pair - b * K;
-    const float tau_in = __ldg(P.temperature + b);
-    const float tau = tau_in > 0.f ? tau_in : 1.f;
-    const float c = kLog2e / tau;
-    const float w = __ldg(P.weights + k);
-    const uint32_t parity = (uint32_t)(it & 1);
+  volatile int *abort_flag = &R.abort;
+  auto pair_c = [&](int it) {
+    const float tau_in = __ldg(P.temperature + (grp + it * ngroups) / K);
+    return kLog2e / (tau_in > 0.f ? tau_in : 1.f);
+  };
 
-    // ---- pass 1: slice statistics, chunk by chunk as the copies land
-    Online ot = online_init(), od = online_init();
-    for (int ch = 0; ch < kTtsChunks; ++ch) {
-      if (!*abort_flag) mbar_wait_bounded(&C.full[ch], parity, abort_flag, &C.status, 2000000000ull);
-      if (*abort_flag) break;
-      const int v0 = min(nvec, ch * cvec), v1 = min(nvec, v0 + cvec);
-      for (int j = v0 + tid; j < v1; j += kTtsThreads) {
-        online_add_vec2<E>(ot, tv[j], c);
-        online_add_vec2<E>(od, dv[j], c);
-      }
-    }
-    MS mt = online_final(ot), md = online_final(od);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const MS a = {__shfl_xor_sync(0xffffffffu, mt.m, o), __shfl_xor_sync(0xffffffffu, mt.S, o)};
-      const MS d = {__shfl_xor_sync(0xffffffffu, md.m, o), __shfl_xor_sync(0xffffffffu, md.S, o)};
-      mt = ms_merge(mt, a, c);
-      md = ms_merge(md, d, c);
-    }
-    if (lane == 0) {
-      C.wt[warp] = mt;
-      C.wd[warp] = md;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      MS a = C.wt[0], d = C.wd[0];
-      for (int i = 1; i < kTtsWarps; ++i) {
-        a = ms_merge(a, C.wt[i], c);
-        d = ms_merge(d, C.wd[i], c);
-      }
-      C.stats[it & 1] = make_float4(a.m, a.S, d.m, d.S);
-    }
-    // every slice's statistics of this pair, and every KL partial of the
-    // previous pair, are published
-    cluster_sync();
-    if (rank == 0 && tid == 0 && prev_b >= 0) {
-      float sum = 0.f, bad = 0.f;
-      for (int r = 0; r < cs; ++r) {
-        const float4 v = ld_shared_cluster_f4(mapa_shared(&C.klpart[(it - 1) & 1], (uint32_t)r));
-        sum += v.x;
-        bad += v.y;
-      }
-      P.out_kl[(size_t)prev_b * K + prev_k] = bad > 0.f ? __int_as_float(0x7fc00000) : prev_w * sum;
-    }
-    mt = {-INFINITY, 0.f};
-    md = {-INFINITY, 0.f};
-    for (int r = 0; r < cs; ++r) {  // rank order: identical in every CTA
-      const float4 v = ld_shared_cluster_f4(mapa_shared(&C.stats[it & 1], (uint32_t)r));
-      mt = ms_merge(mt, MS{v.x, v.y}, c);
-      md = ms_merge(md, MS{v.z, v.w}, c);
-    }
-    const PairConst pc = pair_constants(mt, md, tau);
-    const float at = -fmaf(mt.m, c, log2f(mt.S)), ad = -fmaf(md.m, c, log2f(md.S));
-    const float wg = w * pc.invh;
-    const bool ok = !*abort_flag;
-    // packed constants; the lo parts of 1/tau and K0 move d by at most a few
-    // fp32 ulps of |z_t - z_d| / tau, i.e. the gradient by that times p_v
-    const float2 cc2 = make_float2(c, c), at2 = make_float2(at, at), invh2 = make_float2(pc.invh, pc.invh);
-    const float2 nK0 = make_float2(-(pc.K0h + pc.K0l), -(pc.K0h + pc.K0l)), neg1 = make_float2(-1.f, -1.f);
-    const float2 c120 = make_float2(-1.f / 120.f, -1.f / 120.f), c24 = make_float2(1.f / 24.f, 1.f / 24.f);
-    const float2 c6 = make_float2(-1.f / 6.f, -1.f / 6.f), half2 = make_float2(0.5f, 0.5f);
-    const float2 nlog2e = make_float2(-kLog2e, -kLog2e), wg2 = make_float2(wg, wg);
-    float2 acc2 = make_float2(0.f, 0.f);
-
-    // ---- pass 2: KL terms and the gradient from shared memory, chunk by
-    // chunk; each finished chunk is handed to the next pair's copy
-    uint16_t *grow = P.out_grad ? P.out_grad + ((size_t)b * K + k) * (size_t)V + e0 : nullptr;
-    for (int ch = 0; ch < kTtsChunks; ++ch) {
-      const int v0 = min(nvec, ch * cvec), v1 = min(nvec, v0 + cvec);
-      if (ok)
-        for (int j = v0 + tid; j < v1; j += kTtsThreads) {
-          const uint4 xt = tv[j], xd = dv[j];
-          float g[kPer];
-#pragma unroll
-          for (int e = 0; e < kPer; e += 2) {
-            // two elements per instruction; d = ln p - ln q, p e^-d = q
-            const float2 zt = make_float2(E::get(xt, e), E::get(xt, e + 1));
-            const float2 zd = make_float2(E::get(xd, e), E::get(xd, e + 1));
-            float2 p = __ffma2_rn(zt, cc2, at2);
-            p.x = ex2_approx(p.x);
-            p.y = ex2_approx(p.y);
-            const float2 d = __ffma2_rn(__ffma2_rn(zd, neg1, zt), invh2, nK0);
-            float2 poly = __ffma2_rn(d, c120, c24);
-            poly = __ffma2_rn(d, poly, c6);
-            poly = __ffma2_rn(d, poly, half2);
-            const float2 phi_s = __fmul2_rn(__fmul2_rn(d, d), poly);  // e^-d - 1 + d, small |d|
-            float2 ex = __fmul2_rn(d, nlog2e);
-            ex.x = ex2_approx(ex.x);
-            ex.y = ex2_approx(ex.y);
-            const float2 em1 = __fadd2_rn(ex, neg1);  // e^-d - 1
-            const float2 phl = __fadd2_rn(em1, d);
-            const float2 phi = make_float2(fabsf(d.x) < 0.25f ? phi_s.x : phl.x, fabsf(d.y) < 0.25f ? phi_s.y : phl.y);
-            float2 tkl = __fmul2_rn(p, phi), tg = __fmul2_rn(p, em1);
-            if (!(p.x > 0.f) || !(p.y > 0.f)) {  // z_t = -inf: the limits of both terms are q
-              if (!(p.x > 0.f)) tkl.x = tg.x = ex2_approx(fmaf(zd.x, c, ad));
-              if (!(p.y > 0.f)) tkl.y = tg.y = ex2_approx(fmaf(zd.y, c, ad));
-            }
-            acc2 = __fadd2_rn(acc2, tkl);
-            const float2 gg = __fmul2_rn(wg2, tg);
-            g[e] = gg.x;
-            g[e + 1] = gg.y;
-          }
-          if (grow) {
-            if (kPer == 8) {
-              uint4 o;
-              o.x = bf16x2_rn(g[0], g[1]);
-              o.y = bf16x2_rn(g[2], g[3]);
-              o.z = bf16x2_rn(g[4], g[5]);
-              o.w = bf16x2_rn(g[6], g[7]);
-              __stcs(reinterpret_cast<uint4 *>(grow) + j, o);
-            } else {
-              uint2 o;
-              o.x = bf16x2_rn(g[0], g[1]);
-              o.y = bf16x2_rn(g[2], g[3]);
-              __stcs(reinterpret_cast<uint2 *>(grow) + j, o);
-            }
-          }
+  if (warp < kGrpWarps) {
+    // ---------------- compute warps: chunk cw, thread ct of its owners
+    const int cw = warp / kChunkWarps;
+    const int ct = tid - cw * kChunkThreads;
+    const int v0 = min(nvec, cw * cvec), v1 = min(nvec, v0 + cvec);
+    auto stats = [&](int it) -> MinT {  // pass 1 of pair it over this thread's vectors
+      const float c = pair_c(it);
+      const int bi = it % nb;
+      const uint4 *tv = reinterpret_cast<const uint4 *>(ring + (size_t)bi * 2 * slice_bytes);
+      const uint4 *dv = reinterpret_cast<const uint4 *>(ring + (size_t)bi * 2 * slice_bytes + slice_bytes);
+      Online ot = lazy_init(), od = lazy_init();
+      MinT zmin = E::min_init();
+      if (!*abort_flag) wait_copy(&R.full[bi][cw], (uint32_t)((it / nb) & 1), abort_flag, status, 256u);
+      if (!*abort_flag) pass1_chunk<E, kChunkThreads>(tv, dv, v0, v1, ct, true, c, ot, od, zmin);
+      const MS mt = online_final(ot), md = online_final(od);
+      R.tstat[it & 1][tid] = make_float4(mt.m, mt.S, md.m, md.S);
+      mbar_arrive(&R.stat_bar[it & 1]);
+      return zmin;
+    };
+    MinT zcur = npairs_g > 0 ? stats(0) : E::min_init();
+    for (int it = 0; it < npairs_g; ++it) {
+      const MinT znext = it + 1 < npairs_g ? stats(it + 1) : E::min_init();
+      const int pair = grp + it * ngroups;
+      const int b = pair / K, k = pair - b * K;
+      const int slot = it & (kGrpSlots - 1);
+      mbar_wait_local(&R.const_bar[slot], (uint32_t)((it / kGrpSlots) & 1), status, 256u);
+      const Pass2Const pk = R.pc[slot];
+      const bool ok = R.pc_ok[slot] != 0 && !*abort_flag;
+      const bool fast = pass2_fast_ok<E>(pk, zcur);
+      float2 acc2 = make_float2(0.f, 0.f);
+      const int bi = it % nb;
+      const uint4 *tv = reinterpret_cast<const uint4 *>(ring + (size_t)bi * 2 * slice_bytes);
+      const uint4 *dv = reinterpret_cast<const uint4 *>(ring + (size_t)bi * 2 * slice_bytes + slice_bytes);
+      uint16_t *grow = P.out_grad ? P.out_grad + ((size_t)b * K + k) * (size_t)V + e0 : nullptr;
+      if (ok && fast) pass2_chunk<E, kChunkThreads, true>(tv, dv, v0, v1, ct, pk, acc2, grow);
+      else if (ok) pass2_chunk<E, kChunkThreads, false>(tv, dv, v0, v1, ct, pk, acc2, grow);
+      __syncwarp();
+      if (lane == 0) {  // this warp is done with its chunk; the last owner refills it
+        const uint32_t done = atom_add_acq_rel_cta(&R.released[bi][cw], 1u);
+        if (done == (uint32_t)kChunkWarps * (uint32_t)(it / nb + 1) - 1u && !*abort_flag) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue(it + nb, cw);
         }
-      __syncthreads();  // chunk ch is no longer read
-      if (tid == 0 && !*abort_flag) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(it + 1, ch);
       }
+      float part = acc2.x + acc2.y;
+      if (!fast && pk.fold) part *= pk.wg;  // the scale of the fast path's terms
+      if (!ok) part = __int_as_float(0x7fc00000);
+      R.tkl[it & 1][tid] = part;
+      mbar_arrive(&R.kl_bar[it & 1]);
+      zcur = znext;
     }
-    const float acc = warp_sum(acc2.x + acc2.y);
-    if (lane == 0) C.wk[warp] = acc;
-    __syncthreads();
-    if (tid == 0) {
-      float sum = 0.f;
-      for (int i = 0; i < kTtsWarps; ++i) sum += C.wk[i];
-      C.klpart[it & 1] = make_float4(sum, ok ? 0.f : 1.f, 0.f, 0.f);
+  } else {
+    // ---------------- coordinator warp
+    auto publish = [&](int it) {  // the CTA's entry of pair it
+      const float c = pair_c(it);
+      mbar_wait_local(&R.stat_bar[it & 1], (uint32_t)((it >> 1) & 1), status, 512u);
+      // lane l merges the threads l + 32 j, j < 16, as a tree (depth 4)
+      constexpr int kPerLane = kGrpCompute / 32;
+      MS t[kPerLane], d[kPerLane];
+#pragma unroll
+      for (int j = 0; j < kPerLane; ++j) {
+        const float4 v = R.tstat[it & 1][lane + 32 * j];
+        t[j] = MS{v.x, v.y};
+        d[j] = MS{v.z, v.w};
+      }
+#pragma unroll
+      for (int h = 1; h < kPerLane; h <<= 1)
+#pragma unroll
+        for (int j = 0; j + h < kPerLane; j += 2 * h) {
+          t[j] = ms_merge(t[j], t[j + h], c);
+          d[j] = ms_merge(d[j], d[j + h], c);
+        }
+      MS mt = t[0], md = d[0];
+      warp_merge2(mt, md, c);
+      unsigned long long *rec = g_stat + ((size_t)(it & (kGrpSlots - 1)) * kTtsMaxCtas + cta) * 4;
+      if (lane == 0) {
+        const float nan = __int_as_float(0x7fc00000);  // after an abort: the group's constants become NaN
+        const uint32_t tg = tag_of(it);
+        const bool bad = *abort_flag != 0;
+        st_words2(rec, tagged(bad ? nan : mt.m, tg), tagged(bad ? nan : mt.S, tg));
+        st_words2(rec + 2, tagged(bad ? nan : md.m, tg), tagged(bad ? nan : md.S, tg));
+      }
+    };
+    auto gather = [&](int it) {  // the group's entries of pair it -> the CTA's constants
+      const int pair = grp + it * ngroups;
+      const int b = pair / K, k = pair - b * K;
+      const float tau_in = __ldg(P.temperature + b);
+      const float tau = tau_in > 0.f ? tau_in : 1.f;
+      const float c = kLog2e / tau;
+      const float w = __ldg(P.weights + k);
+      const int slot = it & (kGrpSlots - 1);
+      unsigned long long rw[4];
+      const bool got =
+          poll_records<4>(g_stat + ((size_t)slot * kTtsMaxCtas + (size_t)grp * G) * 4, G, lane, tag_of(it), rw, status);
+      MS mt = {-INFINITY, 0.f}, md = {-INFINITY, 0.f};
+      if (lane < G) {
+        mt = MS{untag(rw[0]), untag(rw[1])};
+        md = MS{untag(rw[2]), untag(rw[3])};
+      }
+      warp_merge2(mt, md, c);
+      if (lane == 0) {
+        const Pass2Const pk = pass2_constants(mt, md, tau, c, w);
+        R.pc[slot] = pk;
+        R.scale[slot] = pk.fold ? w / pk.wg : w;
+        R.pc_ok[slot] = got ? 1 : 0;
+        if (!got) *abort_flag = 1;
+        mbar_arrive(&R.const_bar[slot]);
+      }
+    };
+    auto klsum = [&](int it) {  // the CTA's KL partial of pair it
+      mbar_wait_local(&R.kl_bar[it & 1], (uint32_t)((it >> 1) & 1), status, 512u);
+      constexpr int kPerLane = kGrpCompute / 32;
+      float v[kPerLane];
+#pragma unroll
+      for (int j = 0; j < kPerLane; ++j) v[j] = R.tkl[it & 1][lane + 32 * j];
+#pragma unroll
+      for (int h = 1; h < kPerLane; h <<= 1)
+#pragma unroll
+        for (int j = 0; j + h < kPerLane; j += 2 * h) v[j] += v[j + h];
+      const float s = warp_sum(v[0]);
+      if (lane == 0) st_word(g_kl + (size_t)(it & (kGrpSlots - 1)) * kTtsMaxCtas + cta, tagged(s, tag_of(it)));
+    };
+    auto klgather = [&](int it) {  // rank 0: the group's partials of pair it -> out_kl
+      const int slot = it & (kGrpSlots - 1);
+      unsigned long long w[4];
+      const bool got = poll_records<1>(g_kl + (size_t)slot * kTtsMaxCtas + (size_t)grp * G, G, lane, tag_of(it), w,
+                                       status);
+      const float s = warp_sum(lane < G ? untag(w[0]) : 0.f);
+      if (lane == 0) P.out_kl[grp + it * ngroups] = got ? R.scale[slot] * s : __int_as_float(0x7fc00000);
+    };
+    if (npairs_g > 0) publish(0);
+    for (int it = 0; it < npairs_g; ++it) {
+      gather(it);
+      if (it + 1 < npairs_g) publish(it + 1);
+      if (it >= 1) klsum(it - 1);
+      if (rank == 0 && it >= 2) klgather(it - 2);
     }
-    prev_b = b;
-    prev_k = k;
-    prev_w = w;
+    if (npairs_g > 0) klsum(npairs_g - 1);
+    if (rank == 0)
+      for (int it = max(0, npairs_g - 2); it < npairs_g; ++it) klgather(it);
   }
-  cluster_sync();  // the last pair's KL partials are published
-  if (rank == 0 && tid == 0 && prev_b >= 0) {
-    float sum = 0.f, bad = 0.f;
-    for (int r = 0; r < cs; ++r) {
-      const float4 v = ld_shared_cluster_f4(mapa_shared(&C.klpart[(it - 1) & 1], (uint32_t)r));
-      sum += v.x;
-      bad += v.y;
-    }
-    P.out_kl[(size_t)prev_b * K + prev_k] = bad > 0.f ? __int_as_float(0x7fc00000) : prev_w * sum;
-  }
-  cluster_sync();  // no CTA leaves while rank 0 may still read its shared memory
-  if (tid == 0 && *abort_flag) {  // copies still in flight: wait for them (bounded)
+  __syncthreads();
+  if (tid == 0 && *abort_flag) {  // copies that were never waited for (bounded)
     const uint64_t t0 = global_ns();
-    for (int ch = 0; ch < kTtsChunks; ++ch)
-      while (!mbar_try_wait(&C.full[ch], (uint32_t)(it & 1)) && global_ns() - t0 < 2000000000ull) {
-      }
+    for (int bi = 0; bi < nb; ++bi)
+      for (int ch = 0; ch < kTtsChunks; ++ch)
+        if (R.issued[bi][ch])
+          while (!mbar_try_wait(&R.full[bi][ch], (R.issued[bi][ch] - 1u) & 1u) && global_ns() - t0 < kTtsWaitNs) {
+          }
   }
 }
 
@@ -574,45 +937,58 @@ __global__ void __launch_bounds__(kTtsThreads, 1) tts_cluster_kernel(const TtsPa
 using namespace sv;
 
 namespace {
-// Cluster configuration for one (V, element size): the cluster size with the
-// most SMs resident, slices of S elements, one or two buffers.
+// Launch configuration for one (V, dtype): groups whose slices fit three
+// resident buffers (else two), as many CTAs per SM as the occupancy query
+// allows, the grid a whole number of groups; among the five smallest groups
+// that fit, the one that leaves the fewest CTA slots idle.
 struct TtsCfg {
-  int cs, S, nbuf, clusters;
+  int G, S, nb, ctas;
   size_t smem;
 };
 
-bool tts_cluster_cfg_uncached(int V, int esz, int dtype, TtsCfg *out) {
-  const size_t kSmemMax = 220 * 1024;
-  const size_t head = ((sizeof(ClusterSmem) + 127) / 128) * 128;
-  TtsCfg best{0, 0, 0, 0, 0};
-  for (int cs : {8, 4, 2}) {
-    const int unit = 16 / esz;
-    const int S = ((V + cs - 1) / cs + unit - 1) / unit * unit;
-    const size_t smem = head + 2 * (size_t)S * esz;
-    if (smem > kSmemMax) continue;
-    const void *fn = dtype == SV_BF16 ? (const void *)tts_cluster_kernel<SV_BF16> : (const void *)tts_cluster_kernel<SV_FP32>;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return false;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cs, 1, 1);
-    cfg.blockDim = dim3(kTtsThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = cs;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int ncl = 0;
-    if (cudaOccupancyMaxActiveClusters(&ncl, fn, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      continue;
+bool tts_group_cfg_uncached(int V, int esz, int dtype, int sms, TtsCfg *out) {
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return false;
+  const size_t kSmemMax = (size_t)optin;
+  const int unit = 16 / esz;
+  const size_t head = ((sizeof(GroupSmem) + 127) / 128) * 128;
+  const void *fn = dtype == SV_BF16 ? (const void *)tts_group_kernel<SV_BF16> : (const void *)tts_group_kernel<SV_FP32>;
+  for (int nb : {3, 2}) {
+    TtsCfg best{0, 0, 0, 0, 0};
+    long long best_slots = 0;
+    int tried = 0;
+    for (int G = 1; G <= kTtsMaxGroup && tried < 5; ++G) {
+      const int S = ((V + G - 1) / G + unit - 1) / unit * unit;
+      if ((long long)(G - 1) * S >= V) continue;  // every rank holds part of the row
+      const size_t smem = head + (size_t)nb * 2 * (size_t)S * esz;
+      if (smem > kSmemMax) continue;
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+      }
+      int nper = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nper, fn, kGrpThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+      }
+      long long slots = (long long)nper * sms;
+      if (slots > kTtsMaxCtas) slots = kTtsMaxCtas;
+      const long long ctas = slots / G * G;
+      if (ctas < G) continue;
+      ++tried;
+      if (ctas > best_slots) {
+        best_slots = ctas;
+        best = TtsCfg{G, S, nb, (int)ctas, smem};
+      }
     }
-    if (ncl * cs > best.clusters * best.cs) best = TtsCfg{cs, S, 1, ncl, smem};
+    if (best.G) {
+      *out = best;
+      return true;
+    }
   }
-  if (!best.cs) return false;
-  *out = best;
-  return true;
+  return false;
 }
 
 // small per-process cache keyed by (device, V, dtype)
@@ -623,8 +999,9 @@ struct TtsCacheEnt {
 };
 TtsCacheEnt g_tts_cache[16];
 int g_tts_n = 0;
+std::atomic<uint32_t> g_tts_gen{0};
 
-bool tts_cluster_cfg(int V, int esz, int dtype, TtsCfg *out) {
+bool tts_group_cfg(int V, int esz, int dtype, int sms, TtsCfg *out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   std::lock_guard<std::mutex> lk(g_tts_mu);
@@ -634,7 +1011,7 @@ bool tts_cluster_cfg(int V, int esz, int dtype, TtsCfg *out) {
       return g_tts_cache[i].ok != 0;
     }
   TtsCfg cfg{};
-  const bool ok = tts_cluster_cfg_uncached(V, esz, dtype, &cfg);
+  const bool ok = tts_group_cfg_uncached(V, esz, dtype, sms, &cfg);
   TtsCacheEnt &e = g_tts_cache[g_tts_n < 16 ? g_tts_n++ : 15];
   e = TtsCacheEnt{dev, V, dtype, ok ? 1 : 0, cfg};
   *out = cfg;
@@ -642,11 +1019,15 @@ bool tts_cluster_cfg(int V, int esz, int dtype, TtsCfg *out) {
 }
 }  // namespace
 
+extern "C" size_t sv_tts_workspace_bytes(void) { return kTtsWsBytes; }
+
 extern "C" sv_status_t sv_tts_signal(int B, int K, int V, sv_dtype_t dtype, const void *target_logits,
                                      const void *draft_logits, const float *temperature, const float *weights,
-                                     float *out_kl, uint16_t *out_grad, void *stream) {
+                                     float *out_kl, uint16_t *out_grad, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
   if (B < 0 || B > (1 << 20) || K < 0 || K > SV_MAX_K || V < 1 || V > SV_MAX_V) return SV_ERR_INVALID;
   if (dtype != SV_BF16 && dtype != SV_FP32) return SV_ERR_INVALID;
+  if (!workspace || workspace_bytes < kTtsWsBytes || !host_aligned(workspace, 256)) return SV_ERR_WORKSPACE;
   if ((long long)B * K == 0) return SV_OK;
   if (!target_logits || !draft_logits || !temperature || !weights || !out_kl) return SV_ERR_INVALID;
   const int esz = dtype == SV_BF16 ? 2 : 4;
@@ -659,27 +1040,26 @@ extern "C" sv_status_t sv_tts_signal(int B, int K, int V, sv_dtype_t dtype, cons
   TtsParams P{B, K, V, (int)dtype, target_logits, draft_logits, temperature, weights, out_kl, out_grad};
   const long long pairs = (long long)B * K;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the cluster path wants 16-byte aligned rows and slices
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 4, st);  // this call's status word
+  if (e != cudaSuccess) return host_cuda_status(e);
+  // the group kernel wants 16-byte aligned rows and slices
   const bool aligned16 = ((size_t)V * esz) % 16 == 0 && host_aligned(target_logits, 16) &&
                          host_aligned(draft_logits, 16) && (!out_grad || (host_aligned(out_grad, 16) && V % 8 == 0));
   TtsCfg cfg;
-  if (aligned16 && tts_cluster_cfg(V, esz, (int)dtype, &cfg)) {
-    long long ncl = (pairs < cfg.clusters) ? pairs : cfg.clusters;
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3((unsigned)(ncl * cfg.cs), 1, 1);
-    lc.blockDim = dim3(kTtsThreads, 1, 1);
-    lc.dynamicSmemBytes = cfg.smem;
-    lc.stream = st;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = cfg.cs;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    lc.attrs = &attr;
-    lc.numAttrs = 1;
-    cudaError_t e = dtype == SV_BF16 ? cudaLaunchKernelEx(&lc, tts_cluster_kernel<SV_BF16>, P, cfg.S)
-                                     : cudaLaunchKernelEx(&lc, tts_cluster_kernel<SV_FP32>, P, cfg.S);
-    return host_cuda_status(e);
+  if (aligned16 && tts_group_cfg(V, esz, (int)dtype, sms, &cfg)) {
+    const long long ngroups = pairs < cfg.ctas / cfg.G ? pairs : cfg.ctas / cfg.G;
+    const void *fn =
+        dtype == SV_BF16 ? (const void *)tts_group_kernel<SV_BF16> : (const void *)tts_group_kernel<SV_FP32>;
+    // the occupancy queries of other configurations may have left a smaller limit
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
+    if (e != cudaSuccess) return host_cuda_status(e);
+    uint32_t gen = g_tts_gen.fetch_add(1u) + 1u;
+    while ((uint32_t)(gen << 1) == 0u) gen = g_tts_gen.fetch_add(1u) + 1u;  // tag 0 would match a zeroed workspace
+    const GroupArgs A{cfg.G, cfg.S, cfg.nb, gen, static_cast<unsigned char *>(workspace)};
+    const unsigned grid = (unsigned)(ngroups * cfg.G);
+    if (dtype == SV_BF16) tts_group_kernel<SV_BF16><<<grid, kGrpThreads, cfg.smem, st>>>(P, A);
+    else tts_group_kernel<SV_FP32><<<grid, kGrpThreads, cfg.smem, st>>>(P, A);
+    return host_cuda_status(cudaGetLastError());
   }
   const int grid = (int)(pairs < sms ? pairs : sms);
   if (dtype == SV_BF16) tts_kernel<SV_BF16><<<grid, kTtsThreads, 0, st>>>(P);

@@ -105,3 +105,29 @@ def test_no_gpu_means_an_error_not_a_fallback(lib):
         pytest.skip("a GPU is present")
     # valid host arguments reach the device query, which fails loudly without a GPU
     assert _verify(lib) in (2, 3)
+
+
+def _tts(lib, B=2, K=2, V=64, dtype=1, tgt=0x10000, drf=0x20000, tau=0x40000, wts=0x50000, kl=0x60000,
+         grad=None, ws=0x100000, wsb=None):
+    P = ctypes.c_void_p
+    if wsb is None:
+        wsb = lib.sv_tts_workspace_bytes()
+    return lib.sv_tts_signal(B, K, V, dtype, P(tgt) if tgt else None, P(drf) if drf else None,
+                             P(tau) if tau else None, P(wts) if wts else None, P(kl) if kl else None,
+                             P(grad) if grad else None, P(ws) if ws else None, wsb, None)
+
+
+def test_tts_host_argument_checks(lib):
+    INVALID, WORKSPACE = 1, 7
+    n = lib.sv_tts_workspace_bytes()
+    assert n > 0 and n % 256 == 0 and n < 1 << 20
+    assert _tts(lib, K=17) == INVALID
+    assert _tts(lib, V=0) == INVALID
+    assert _tts(lib, dtype=5) == INVALID
+    assert _tts(lib, ws=0) == WORKSPACE
+    assert _tts(lib, ws=0x100010) == WORKSPACE           # not 256-byte aligned
+    assert _tts(lib, wsb=n - 1) == WORKSPACE
+    assert _tts(lib, B=0) == 0                           # nothing to do
+    assert _tts(lib, tgt=0) == INVALID
+    assert _tts(lib, kl=0) == INVALID
+    assert _tts(lib, grad=0x70001) == INVALID            # gradient not aligned to 2 bytes

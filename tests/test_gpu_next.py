@@ -143,7 +143,10 @@ def _tts_case(w, weights, pairs=None):
     for b, k in pairs:
         r = oracle.tts_signal(t[b:b + 1, k:k + 1], d[b:b + 1, k:k + 1], tau[b:b + 1], [weights[k]])
         ko = r["kl"][0, 0]
-        assert abs(kl[b, k] - ko) <= 1e-4 * abs(ko) + 1e-9, (b, k, kl[b, k], ko)
+        if np.isinf(ko):  # a draft logit of -inf where p > 0
+            assert kl[b, k] == ko, (b, k, kl[b, k], ko)
+        else:
+            assert abs(kl[b, k] - ko) <= 1e-4 * abs(ko) + 1e-9, (b, k, kl[b, k], ko)
         go = r["grad"][0, 0]
         gg = grad[b, k].float().cpu().numpy()
         tb = tau[b] if tau[b] > 0 else 1.0
@@ -154,7 +157,7 @@ def _tts_case(w, weights, pairs=None):
         # bf16 rounding, plus the fp32 normalisation of p and q (their sums
         # over the row are kept to a few 1e-7): the error of q_v - p_v is
         # bounded relative to the larger of the two
-        tol = 1.01 * 2.0**-8 * np.abs(go) + 2e-6 * weights[k] / tb * np.maximum(p, q) + 1e-38
+        tol = 1.01 * 2.0**-8 * np.abs(go) + 2e-6 * abs(weights[k]) / tb * np.maximum(p, q) + 1e-38
         bad = np.abs(gg - go) > tol
         assert not bad.any(), (b, k, np.nonzero(bad)[0][:5], gg[bad][:5], go[bad][:5])
     return kl
@@ -171,6 +174,37 @@ def test_tts_tiny_and_unaligned():
         ww = synth.Workload("u", 5, 3, V, dt, z.to(dt).contiguous(), dd.to(dt).contiguous(),
                             torch.zeros((5, 3), dtype=torch.int32), torch.ones(5))
         _tts_case(ww, [1.0, 0.5, 0.25])
+
+
+def _tts_rows(B, K, V, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    z = torch.randn((B, K + 1, V), generator=g) * 2
+    dd = z[:, :K] + torch.randn((B, K, V), generator=g) * 0.5
+    return synth.Workload("t", B, K, V, dtype, z.to(dtype).contiguous(), dd.to(dtype).contiguous(),
+                          torch.zeros((B, K), dtype=torch.int32), torch.ones(B))
+
+
+def test_tts_two_resident_buffers():
+    # V = 151936 bf16: a cluster of 8 holds two pair slices per CTA, not three
+    _tts_case(_tts_rows(3, 3, 151936, torch.bfloat16, 11), [1.0, 0.7, 0.5])
+
+
+def test_tts_single_buffer_fp32():
+    # V = 128256 fp32: one pair slice per CTA (three CTAs per SM)
+    _tts_case(_tts_rows(2, 2, 128256, torch.float32, 12), [1.0, 0.6])
+
+
+def test_tts_masked_logits_and_degenerate_weights():
+    # target logits of -inf and far below the rest (p = 0 or an underflow, the
+    # warps holding them take the general path), a draft logit of -inf where
+    # p > 0 (KL = +inf), a zero and a negative weight
+    w = _tts_rows(4, 3, 32000, torch.bfloat16, 13)
+    w.target[0, 0, :300] = float("-inf")
+    w.target[1, 1, 4000:4064] = -3.0e4
+    w.target[2, 2, 31990:] = float("-inf")
+    w.draft[3, 0, 7] = float("-inf")
+    w.temperature = torch.tensor([1.0, 0.5, 1.7, 1.0])
+    _tts_case(w, [1.0, 0.0, -0.5])
 
 
 def test_tts_identical_rows_give_zero():
