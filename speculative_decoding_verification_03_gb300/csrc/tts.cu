@@ -535,13 +535,14 @@ __device__ __forceinline__ void pass2_chunk(const uint4 *tv, const uint4 *dv, in
       poly = __ffma2_rn(d, poly, c6);
       poly = __ffma2_rn(d, poly, half2);  // (e^-d - 1 + d) / d^2 to fifth order
       if (kFast) {
-        const float2 tg = __ffma2_rn(p, ex, make_float2(-p.x, -p.y));  // (w / tau) (q - p)
-        const float2 t = __fmul2_rn(p, d);
-        const float2 tl = __fadd2_rn(t, tg);
-        const float2 ts = __fmul2_rn(t, __fmul2_rn(d, poly));
-        acc2 = __fadd2_rn(acc2, make_float2(fabsf(d.x) < 0.25f ? ts.x : tl.x, fabsf(d.y) < 0.25f ? ts.y : tl.y));
-        g[e] = tg.x;
-        g[e + 1] = tg.y;
+        // scalar from here: the exponentials come out of the SFU one by one
+        const float2 dp = __fmul2_rn(d, poly);
+        const float tgx = fmaf(p.x, ex.x, -p.x), tgy = fmaf(p.y, ex.y, -p.y);  // (w / tau) (q - p)
+        const float tx = p.x * d.x, ty = p.y * d.y;
+        acc2.x += fabsf(d.x) < 0.25f ? tx * dp.x : tx + tgx;
+        acc2.y += fabsf(d.y) < 0.25f ? ty * dp.y : ty + tgy;
+        g[e] = tgx;
+        g[e + 1] = tgy;
       } else {
         const float2 phi_s = __fmul2_rn(__fmul2_rn(d, d), poly);
         const float2 em1 = __fadd2_rn(ex, neg1);  // e^-d - 1
@@ -585,6 +586,7 @@ __device__ __forceinline__ void pass2_chunk(const uint4 *tv, const uint4 *dv, in
 constexpr int kGrpWarps = 16;                        // compute warps
 constexpr int kGrpCompute = kGrpWarps * 32;
 constexpr int kGrpThreads = kGrpCompute + 32;        // + the coordinator warp
+constexpr int kGrpMinBlocks = kGrpWarps >= 16 ? 1 : 16 / kGrpWarps;  // CTAs per SM the registers must allow
 constexpr int kChunkWarps = kGrpWarps / kTtsChunks;  // warps that own a chunk
 constexpr int kChunkThreads = kChunkWarps * 32;
 constexpr int kGrpMaxNb = 3;
@@ -707,7 +709,7 @@ __device__ __forceinline__ bool poll_records(const unsigned long long *rec, int 
 }
 
 template <int kDtype>
-__global__ void __launch_bounds__(kGrpThreads, 1) tts_group_kernel(const TtsParams P, const GroupArgs A) {
+__global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks) tts_group_kernel(const TtsParams P, const GroupArgs A) {
   using E = TtsElems<kDtype>;
   using MinT = typename E::MinT;
   constexpr int kEsz = kDtype == SV_BF16 ? 2 : 4;
@@ -939,8 +941,8 @@ using namespace sv;
 namespace {
 // Launch configuration for one (V, dtype): groups whose slices fit three
 // resident buffers (else two), as many CTAs per SM as the occupancy query
-// allows, the grid a whole number of groups; among the five smallest groups
-// that fit, the one that leaves the fewest CTA slots idle.
+// allows, the grid a whole number of groups; among the groups that fit, the
+// one with the most resident CTAs (then the smallest).
 struct TtsCfg {
   int G, S, nb, ctas;
   size_t smem;
@@ -958,8 +960,7 @@ bool tts_group_cfg_uncached(int V, int esz, int dtype, int sms, TtsCfg *out) {
   for (int nb : {3, 2}) {
     TtsCfg best{0, 0, 0, 0, 0};
     long long best_slots = 0;
-    int tried = 0;
-    for (int G = 1; G <= kTtsMaxGroup && tried < 5; ++G) {
+    for (int G = 1; G <= kTtsMaxGroup; ++G) {
       const int S = ((V + G - 1) / G + unit - 1) / unit * unit;
       if ((long long)(G - 1) * S >= V) continue;  // every rank holds part of the row
       const size_t smem = head + (size_t)nb * 2 * (size_t)S * esz;
@@ -977,7 +978,6 @@ bool tts_group_cfg_uncached(int V, int esz, int dtype, int sms, TtsCfg *out) {
       if (slots > kTtsMaxCtas) slots = kTtsMaxCtas;
       const long long ctas = slots / G * G;
       if (ctas < G) continue;
-      ++tried;
       if (ctas > best_slots) {
         best_slots = ctas;
         best = TtsCfg{G, S, nb, (int)ctas, smem};
