@@ -5,12 +5,14 @@
 //   kl[b][k]      = w_k * KL(p || q)
 //   grad[b][k][v] = w_k * (q_v - p_v) / tau        (bf16; the gradient of
 //                   that term with respect to the draft logits)
-// One CTA per (b, k) row pair at a time, two passes over the pair: online
-// max/sum statistics of both rows, then the per-element KL terms and the
-// gradient; the second pass re-reads the pair from L2.  KL is summed as
-// p (e^-d - 1 + d) with d = ln p - ln q, a sum of non-negative terms taken
-// by a short series for small |d|, so it keeps its relative precision when
-// q is close to p.
+// Two passes over each row pair: the rows' (max, sum) statistics, then the
+// per-element KL terms and the gradient.  tts_group_kernel (16-byte aligned
+// rows) holds each pair in the shared memory of a group of CTAs across both
+// passes, so every row is read from HBM once; tts_kernel (any alignment) runs
+// one CTA per pair and re-reads the pair from L2 in the second pass.  KL is
+// summed as p (e^-d - 1 + d) with d = ln p - ln q, a sum of non-negative
+// terms taken by a short series for small |d|, so it keeps its relative
+// precision when q is close to p.
 #include <atomic>
 #include <cfloat>
 #include <mutex>
@@ -144,27 +146,6 @@ __device__ __forceinline__ void online_add_vec(Online &o, const uint4 &x, float 
     for (int e = 0; e < E::kPer; ++e) o.s += ex2_approx(fmaf(E::get(x, e), c, o.nbh));
   }
 }
-// the same with packed fp32x2 arithmetic (pairs of elements per instruction)
-template <typename E>
-__device__ __forceinline__ void online_add_vec2(Online &o, const uint4 &x, float c) {
-  float vm = E::get(x, 0);
-#pragma unroll
-  for (int e = 1; e < E::kPer; ++e) vm = fmaxf(vm, E::get(x, e));
-  if (vm > o.m) online_raise(o, vm, c);
-  if (o.m > -INFINITY) {
-    const float2 cc = make_float2(c, c), nb = make_float2(o.nbh, o.nbh);
-    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int e = 0; e < E::kPer; e += 2) {
-      float2 t = __ffma2_rn(make_float2(E::get(x, e), E::get(x, e + 1)), cc, nb);
-      t.x = ex2_approx(t.x);
-      t.y = ex2_approx(t.y);
-      acc = __fadd2_rn(acc, t);
-    }
-    o.s += acc.x + acc.y;
-  }
-}
-
 // Lazy reference for the row-pass statistics held in shared memory: the
 // terms are 2^(z c + nbh) with nbh = -m c for a reference m that is raised
 // only when a vector's terms would pass 2^64, which keeps any row's sum far
