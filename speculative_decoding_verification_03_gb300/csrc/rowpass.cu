@@ -1069,6 +1069,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
   uint32_t phase = 0;
   int it = 0;
   float c = 1.f;
+  int rot = 0;  // sample stages: which warps take the extra sub-chunk alternates
   for (;;) {
     if (!mbar_wait_bounded(&S.full[s], phase, abort_flag, P.status, P.timeout_ns)) break;
     const StageHot h = S.hot[s];
@@ -1100,7 +1101,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
       const int n = h.nvec * 16 / kEsz;
       const int nsc = (n + kSubChunk - 1) / kSubChunk;
       float *sub = P.smp.subsum + (size_t)hs.b * P.smp.nsub + h.e0 / kSubChunk;
-      for (int q = warp; q < nsc; q += kConsumerWarps) {
+      // 54 sub-chunks per full stage over 12 warps: half of the warps take a
+      // fifth one, alternately, so that no warp falls behind over a draw
+      for (int q = (warp + rot) % kConsumerWarps; q < nsc; q += kConsumerWarps) {
         const int off = q * kSubChunk + lane * 8;  // element offset inside the stage
         const Raw8 zt = smem_raw8<kDtype>(S.ring[s], off);
         Raw8 zd;
@@ -1109,6 +1112,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
         const float sm = warp_sum(weights_sum8<kDtype>(t, t.kind, off, n, zt, zd));
         if (lane == 0) sub[q] = sm;
       }
+      rot ^= kConsumerWarps / 2;
       const bool last = (h.flags & kFlagLast) != 0;
       const int bb = hs.b;
       __syncwarp();
