@@ -24,6 +24,10 @@
  *    until it is read.  The
  *    kernels never trap: the affected sequence still gets outputs, produced
  *    by the rules stated at each flag.
+ *  - The verification and TTS kernels are persistent (one CTA per SM) and
+ *    their CTAs hand work to one another through bounded waits, so a launch
+ *    expects its CTAs to be resident together: with other kernels holding
+ *    the SMs, a wait can give up (SV_FLAG_TIMEOUT) instead of completing.
  *  - Logits are row-major, the vocabulary innermost and contiguous.  Any
  *    V in [1, SV_MAX_V] is accepted; rows need not be 16-byte aligned (the
  *    ragged ends are read with plain loads), but each logit pointer must be
@@ -145,7 +149,9 @@ size_t sv_workspace_bytes(int B, int K, int V);
  * but in range.
  * Target rows after a sequence's first rejection do not affect any output.
  * When the draft rows are streamed (draft_stats == NULL) they are not read
- * either, apart from at most one row read ahead, whose flags are ignored.
+ * either, apart from rows read ahead of the walk (up to three when the
+ * launch streams under 128 MB of first-pass rows, one under 1 GB, none
+ * above), whose flags are ignored.
  * ---------------------------------------------------------------------- */
 sv_status_t sv_verify(int B, int K, int V, sv_dtype_t dtype,
                       const void *target_logits, const void *draft_logits,
