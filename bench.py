@@ -625,7 +625,9 @@ def run_op(args):
     kernel = dict(budget="av_budget_kernel", post="post_verify_kernel", tts="tts_group_kernel", tree="tree_kernel")[op]
     res_line = dict(metric=unit.replace("/s", " per second") + " (" + op + ")", value=value, unit=unit, n_gpus=1,
                     steps=args.steps, warmup=args.warmup, ms_per_step=mean_ms, higher_is_better=True,
-                    scaling="weak", vs_baseline=None, dtype="f32", data="synthetic",
+                    scaling="weak", vs_baseline=None,
+                    dtype=dict(budget="f32", post="int32", tts="bf16", tree="bf16")[op],  # as the verify line: the inputs'
+                    data="synthetic",
                     ms_p10_p50_p90=[ms[len(ms) // 10], ms[len(ms) // 2], ms[(9 * len(ms)) // 10]],
                     roofline=dict(bound="hbm", kernel=kernel, achieved=achieved, peak=peak, unit="GB/s",
                                   frac=achieved / peak, traffic=None, algorithmic_bytes_per_launch=nbytes,
