@@ -119,7 +119,6 @@ __device__ __forceinline__ uint16_t bf16_rn(float f) { return (uint16_t)(bf16x2_
 struct Online {
   float m, s, nbh, nbl;
 };
-__device__ __forceinline__ Online online_init() { return {-INFINITY, 0.f, 0.f, 0.f}; }
 __device__ __forceinline__ void online_raise(Online &o, float vm, float c) {
   const float nbh = __fmul_rn(-vm, c);
   const float nbl = fmaf(-vm, c, -nbh);
@@ -130,20 +129,50 @@ __device__ __forceinline__ void online_raise(Online &o, float vm, float c) {
   o.nbh = nbh;
   o.nbl = nbl;
 }
-__device__ __forceinline__ void online_add(Online &o, float z, float c) {
-  if (z > o.m) online_raise(o, z, c);
-  if (o.m > -INFINITY) o.s += ex2_approx(fmaf(z, c, o.nbh));
+// The same statistics for tts_kernel, where one thread sums up to ~65K terms
+// of a row (V = 2^24 over 256 threads): each vector's eight terms are added
+// pairwise, and the vector sums go into s with Kahan's compensated addition
+// (cmp holds the low-order part lost by the previous addition), so the
+// thread's sum keeps fp32 precision whatever the row length.
+struct OnlineK {
+  float m, s, cmp, nbh, nbl;
+};
+__device__ __forceinline__ void kahan_add(float &s, float &cmp, float v) {
+  const float y = __fsub_rn(v, cmp);
+  const float t = __fadd_rn(s, y);
+  cmp = __fsub_rn(__fsub_rn(t, s), y);
+  s = t;
 }
-// one 16-byte vector: raise once to the vector's max, then add its terms
+__device__ __forceinline__ OnlineK onlinek_init() { return {-INFINITY, 0.f, 0.f, 0.f, 0.f}; }
+__device__ __forceinline__ void onlinek_raise(OnlineK &o, float vm, float c) {
+  const float nbh = __fmul_rn(-vm, c);
+  const float nbl = fmaf(-vm, c, -nbh);
+  const float f = o.m == -INFINITY ? 0.f : ex2_approx(nbh - o.nbh);
+  o.s = o.m == -INFINITY ? 0.f : o.s * f;
+  o.cmp = o.m == -INFINITY ? 0.f : o.cmp * f;
+  o.m = vm;
+  o.nbh = nbh;
+  o.nbl = nbl;
+}
+__device__ __forceinline__ void onlinek_add(OnlineK &o, float z, float c) {
+  if (z > o.m) onlinek_raise(o, z, c);
+  if (o.m > -INFINITY) kahan_add(o.s, o.cmp, ex2_approx(fmaf(z, c, o.nbh)));
+}
 template <typename E>
-__device__ __forceinline__ void online_add_vec(Online &o, const uint4 &x, float c) {
+__device__ __forceinline__ void onlinek_add_vec(OnlineK &o, const uint4 &x, float c) {
   float vm = E::get(x, 0);
 #pragma unroll
   for (int e = 1; e < E::kPer; ++e) vm = fmaxf(vm, E::get(x, e));
-  if (vm > o.m) online_raise(o, vm, c);
+  if (vm > o.m) onlinek_raise(o, vm, c);
   if (o.m > -INFINITY) {
+    float t[E::kPer];
 #pragma unroll
-    for (int e = 0; e < E::kPer; ++e) o.s += ex2_approx(fmaf(E::get(x, e), c, o.nbh));
+    for (int e = 0; e < E::kPer; ++e) t[e] = ex2_approx(fmaf(E::get(x, e), c, o.nbh));
+#pragma unroll
+    for (int h = 1; h < E::kPer; h <<= 1)
+#pragma unroll
+      for (int e = 0; e + h < E::kPer; e += 2 * h) t[e] += t[e + h];
+    kahan_add(o.s, o.cmp, t[0]);
   }
 }
 // Lazy reference for the row-pass statistics held in shared memory: the
@@ -193,6 +222,9 @@ struct MS {
   float m, S;
 };
 __device__ __forceinline__ MS online_final(const Online &o) { return {o.m, o.s * fmaf(o.nbl, kLn2, 1.f)}; }
+__device__ __forceinline__ MS onlinek_final(const OnlineK &o) {
+  return {o.m, __fsub_rn(o.s, o.cmp) * fmaf(o.nbl, kLn2, 1.f)};
+}
 __device__ __forceinline__ MS ms_merge(MS a, MS b, float c) {
   if (b.m > a.m) {
     const MS t = a;
@@ -252,7 +284,7 @@ __global__ void __launch_bounds__(kTtsThreads, 1) tts_kernel(const TtsParams P) 
     const uint4 *dv = reinterpret_cast<const uint4 *>(drow + (size_t)v0 * kEsz);
 
     // ---- pass 1: online statistics of both rows
-    Online ot = online_init(), od = online_init();
+    OnlineK ot = onlinek_init(), od = onlinek_init();
     for (int base = 0; base < nvec; base += kTtsThreads * kTtsUnroll) {
       uint4 xt[kTtsUnroll], xd[kTtsUnroll];
 #pragma unroll
@@ -267,18 +299,18 @@ __global__ void __launch_bounds__(kTtsThreads, 1) tts_kernel(const TtsParams P) 
       for (int u = 0; u < kTtsUnroll; ++u) {
         const int j = base + u * kTtsThreads + tid;
         if (j < nvec) {
-          online_add_vec<E>(ot, xt[u], c);
-          online_add_vec<E>(od, xd[u], c);
+          onlinek_add_vec<E>(ot, xt[u], c);
+          onlinek_add_vec<E>(od, xd[u], c);
         }
       }
     }
     const int nh = v0, nrest = v0 + (V - v1);  // elements outside the vector span
     for (int i = tid; i < nrest; i += kTtsThreads) {
       const int v = i < nh ? i : v1 + (i - nh);
-      online_add(ot, E::scalar(trow, v), c);
-      online_add(od, E::scalar(drow, v), c);
+      onlinek_add(ot, E::scalar(trow, v), c);
+      onlinek_add(od, E::scalar(drow, v), c);
     }
-    MS mt = online_final(ot), md = online_final(od);
+    MS mt = onlinek_final(ot), md = onlinek_final(od);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const MS a = {__shfl_xor_sync(0xffffffffu, mt.m, o), __shfl_xor_sync(0xffffffffu, mt.S, o)};
@@ -310,11 +342,11 @@ __global__ void __launch_bounds__(kTtsThreads, 1) tts_kernel(const TtsParams P) 
     // log2 p_v = z_t c + at, log2 q_v = z_d c + ad (one FMA each)
     const float at = -fmaf(Mt, c, l2St), ad = -fmaf(Md, c, l2Sd);
     const float wg = w * invtau;
-    float acc = 0.f;
+    float acc = 0.f, acc_c = 0.f;  // Kahan-compensated sum of the thread's KL terms
     // Per element: d = ln p - ln q; the KL term p (e^-d - 1 + d) and the
     // gradient w (q - p) / tau = w p (e^-d - 1) / tau.  For |d| < 1/4 both
     // come from series in d (no cancellation), else from e^-d directly.
-    auto element = [&](float zt, float zd, float &g) {
+    auto element = [&](float zt, float zd, float &g) -> float {
       const float p = ex2_approx(fmaf(zt, c, at));
       const float q = ex2_approx(fmaf(zd, c, ad));
       const float dz = zt - zd;
@@ -330,8 +362,8 @@ __global__ void __launch_bounds__(kTtsThreads, 1) tts_kernel(const TtsParams P) 
       const float em1 = small ? em1_s : e - 1.f;
       const float phi = small ? phi_s : em1 + d;
       // p = 0 (z_t = -inf): the term's limit is q
-      acc += p > 0.f ? p * phi : q;
       g = wg * (p > 0.f ? p * em1 : q);
+      return p > 0.f ? p * phi : q;
     };
     uint16_t *grow = P.out_grad ? P.out_grad + ((size_t)b * K + k) * (size_t)V : nullptr;
     const bool gvec = grow && ((reinterpret_cast<uintptr_t>(grow + v0) & 15) == 0);
@@ -349,9 +381,10 @@ __global__ void __launch_bounds__(kTtsThreads, 1) tts_kernel(const TtsParams P) 
       for (int u = 0; u < kTtsUnroll; ++u) {
         const int j = base + u * kTtsThreads + tid;
         if (j < nvec) {
-          float g[kPer];
+          float g[kPer], kv = 0.f;
 #pragma unroll
-          for (int e = 0; e < kPer; ++e) element(E::get(xt[u], e), E::get(xd[u], e), g[e]);
+          for (int e = 0; e < kPer; ++e) kv += element(E::get(xt[u], e), E::get(xd[u], e), g[e]);
+          kahan_add(acc, acc_c, kv);
           if (grow) {
             const int v = v0 + j * kPer;
             if (gvec && kPer == 8) {
@@ -372,10 +405,10 @@ __global__ void __launch_bounds__(kTtsThreads, 1) tts_kernel(const TtsParams P) 
     for (int i = tid; i < nrest; i += kTtsThreads) {
       const int v = i < nh ? i : v1 + (i - nh);
       float g;
-      element(E::scalar(trow, v), E::scalar(drow, v), g);
+      kahan_add(acc, acc_c, element(E::scalar(trow, v), E::scalar(drow, v), g));
       if (grow) grow[v] = bf16_rn(g);
     }
-    acc = warp_sum(acc);
+    acc = warp_sum(__fsub_rn(acc, acc_c));
     if (lane == 0) s_kl[warp] = acc;
     __syncthreads();
     if (tid == 0) {
@@ -922,8 +955,13 @@ using namespace sv;
 namespace {
 // Launch configuration for one (V, dtype): groups whose slices fit three
 // resident buffers (else two), as many CTAs per SM as the occupancy query
-// allows, the grid a whole number of groups; among the groups that fit, the
-// one with the most resident CTAs (then the smallest).
+// allows, the grid a whole number of groups.  Among the group sizes that
+// fit, the one with the least estimated time per pair and group: a pair
+// costs each CTA about 0.4 us per 16-byte vector step of its slowest thread
+// (ceil(vectors per chunk / threads per chunk), per pass) plus about 2.3 us
+// of per-pair latency (measured on the C3 rows, B=256 K=5 V=128256 bf16:
+// G = 8, three slices, 4 steps: 267 us; G = 10, four slices, 4 steps:
+// 322 us; G = 19, four slices, 2 steps: 501 us).
 struct TtsCfg {
   int G, S, nb, ctas;
   size_t smem;
@@ -940,7 +978,7 @@ bool tts_group_cfg_uncached(int V, int esz, int dtype, int sms, TtsCfg *out) {
   const void *fn = dtype == SV_BF16 ? (const void *)tts_group_kernel<SV_BF16> : (const void *)tts_group_kernel<SV_FP32>;
   for (int nb : {3, 2}) {
     TtsCfg best{0, 0, 0, 0, 0};
-    long long best_slots = 0;
+    double best_cost = 0.0;
     for (int G = 1; G <= kTtsMaxGroup; ++G) {
       const int S = ((V + G - 1) / G + unit - 1) / unit * unit;
       if ((long long)(G - 1) * S >= V) continue;  // every rank holds part of the row
@@ -959,8 +997,11 @@ bool tts_group_cfg_uncached(int V, int esz, int dtype, int sms, TtsCfg *out) {
       if (slots > kTtsMaxCtas) slots = kTtsMaxCtas;
       const long long ctas = slots / G * G;
       if (ctas < G) continue;
-      if (ctas > best_slots) {
-        best_slots = ctas;
+      const int cvec = (S / unit + kTtsChunks - 1) / kTtsChunks;  // 16-byte vectors per chunk
+      const int steps = (cvec + kChunkThreads - 1) / kChunkThreads;
+      const double cost = (0.4 * steps + 2.3) / (double)(ctas / G);
+      if (!best.G || cost < best_cost) {
+        best_cost = cost;
         best = TtsCfg{G, S, nb, (int)ctas, smem};
       }
     }

@@ -184,14 +184,32 @@ def _tts_rows(B, K, V, dtype, seed):
                           torch.zeros((B, K), dtype=torch.int32), torch.ones(B))
 
 
-def test_tts_two_resident_buffers():
-    # V = 151936 bf16: a cluster of 8 holds two pair slices per CTA, not three
+def test_tts_c4_vocabulary():
+    # V = 151936 bf16: another group size and slice length than the C3 rows
     _tts_case(_tts_rows(3, 3, 151936, torch.bfloat16, 11), [1.0, 0.7, 0.5])
 
 
-def test_tts_single_buffer_fp32():
-    # V = 128256 fp32: one pair slice per CTA (three CTAs per SM)
+def test_tts_fp32_rows():
+    # V = 128256 fp32: slices of 16-byte vectors of four elements
     _tts_case(_tts_rows(2, 2, 128256, torch.float32, 12), [1.0, 0.6])
+
+
+def test_tts_wide_rows_two_resident_slices():
+    # V = 700000 bf16: three pair slices per CTA fit no group of at most 32
+    # CTAs, so two do (and fewer pairs than groups)
+    _tts_case(_tts_rows(1, 2, 700000, torch.bfloat16, 14), [1.0, 0.8])
+
+
+def test_tts_maximum_vocabulary():
+    # V = 2^24 bf16 (SV_MAX_V): slices too long for shared memory, so the
+    # kernel that reads each pair twice (the second time from L2) runs
+    V = 1 << 24
+    g = torch.Generator().manual_seed(15)
+    z = torch.randn((1, 2, V), generator=g) * 2
+    d = z[:, :1] + torch.randn((1, 1, V), generator=g) * 0.5
+    w = synth.Workload("t", 1, 1, V, torch.bfloat16, z.to(torch.bfloat16).contiguous(),
+                       d.to(torch.bfloat16).contiguous(), torch.zeros((1, 1), dtype=torch.int32), torch.ones(1))
+    _tts_case(w, [0.9])
 
 
 def test_tts_masked_logits_and_degenerate_weights():
@@ -227,6 +245,20 @@ def test_tts_c3_sampled_pairs():
     pairs = [(int(b), int(k)) for b, k in zip(rng.integers(0, w.B, 12), rng.integers(0, w.K, 12))]
     kl = _tts_case(w, [1.0, 0.9, 0.8, 0.7, 0.6], pairs=pairs)
     assert np.all(np.isfinite(kl)) and np.all(kl >= 0)
+
+
+def test_tts_c3_every_kl():
+    # the full C3 launch (the bench's configuration): every one of the 1280
+    # KL values against the oracle (the gradient is sampled above)
+    w = synth.c3(seed=7, device="cuda")
+    weights = [1.0, 0.9, 0.8, 0.7, 0.6]
+    kl, _ = binding.tts_signal(w.target, w.draft, w.temperature,
+                               torch.tensor(weights, dtype=torch.float32, device="cuda"), want_grad=False)
+    kl = kl.cpu().numpy()
+    t = (synth.logits_np(w.target).astype(np.uint32) << 16).view(np.float32)
+    d = (synth.logits_np(w.draft).astype(np.uint32) << 16).view(np.float32)
+    ko = oracle.tts_signal(t, d, w.temperature.cpu().numpy(), weights, want_grad=False)["kl"]
+    assert np.all(np.abs(kl - ko) <= 1e-4 * np.abs(ko) + 1e-9), np.max(np.abs(kl - ko) / (np.abs(ko) + 1e-9))
 
 
 # ----------------------------------------------------------------------------- tree
