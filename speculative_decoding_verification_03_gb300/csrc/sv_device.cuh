@@ -214,6 +214,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Kahan's compensated addition s += v: cmp holds the low-order part that the
+// previous addition lost (the sum is s - cmp), so a thread's sum of many
+// positive terms keeps fp32 precision however long the row (terms below half
+// an ulp of a plain running sum would be rounded away one by one).
+__device__ __forceinline__ void kahan_add(float &s, float &cmp, float v) {
+  const float y = __fsub_rn(v, cmp);
+  const float t = __fadd_rn(s, y);
+  cmp = __fsub_rn(__fsub_rn(t, s), y);
+  s = t;
+}
+
 // bf16 pair packed in a 32-bit word -> two fp32 values (exact widening).
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

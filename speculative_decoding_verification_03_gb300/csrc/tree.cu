@@ -321,19 +321,23 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
             mt = fmaxf(mt, s_on_t[i].m);
             md = fmaxf(md, s_on_d[i].m);
           }
-          float st = 0.f, sd = 0.f;
+          // a thread's eight terms summed, then added with compensation (long rows)
+          float st = 0.f, sd = 0.f, st_c = 0.f, sd_c = 0.f;
           for (int o = tid; o < noct; o += kTreeThreads) {
             float zt[8], zd[8];
             load8<kS>(trow, P.dtype, V, o << 3, vec, zt);
             load8<kS>(drow, P.dtype, V, o << 3, vec, zd);
+            float vt = 0.f, vd = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              if (mt > -INFINITY) st += ex2_approx((zt[e] - mt) * c);
-              if (md > -INFINITY) sd += ex2_approx((zd[e] - md) * c);
+              if (mt > -INFINITY) vt += ex2_approx((zt[e] - mt) * c);
+              if (md > -INFINITY) vd += ex2_approx((zd[e] - md) * c);
             }
+            kahan_add(st, st_c, vt);
+            kahan_add(sd, sd_c, vd);
           }
-          st = warp_sum(st);
-          sd = warp_sum(sd);
+          st = warp_sum(__fsub_rn(st, st_c));
+          sd = warp_sum(__fsub_rn(sd, sd_c));
           __syncthreads();  // the maxima are read
           if (lane == 0) {
             s_on_t[warp].s = st;
@@ -407,18 +411,20 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
             break;
           }
           // rejected: the residual's mass R_{j+1}
-          float part = 0.f;
+          float part = 0.f, part_c = 0.f;
           for (int o = tid; o < noct; o += kTreeThreads) {
             float zt[8], zd[8];
             load8<kS>(trow, P.dtype, V, o << 3, vec, zt);
             load8<kS>(drow, P.dtype, V, o << 3, vec, zd);
+            float v8 = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float qv = D.qz(zd[e]);
-              part += fmaxf(D.pjz(zt[e], qv) - qv, 0.f);
+              v8 += fmaxf(D.pjz(zt[e], qv) - qv, 0.f);
             }
+            kahan_add(part, part_c, v8);
           }
-          const float R = block_sum(part, s_red);
+          const float R = block_sum(__fsub_rn(part, part_c), s_red);
           if (R > 0.f) {
             D.a += 1.f / D.invZ;
             D.invZ /= R;
@@ -518,15 +524,17 @@ __global__ void __launch_bounds__(kTreeThreads, 1) tree_kernel(const TreeParams 
               if (lane == 0) s_tok = c2 != INT_MAX ? c2 : (back >= 0 ? back : 0);
             }
           } else {
-            float ws = 0.f;
+            float ws = 0.f, ws_c = 0.f;
             for (int v = s0 + lane * 8; v < s1; v += 256) {
               float zt[8], zd[8];
               load8<kS>(trow, P.dtype, s1, v, vec, zt);
               load8<kS>(drow, P.dtype, s1, v, vec, zd);
+              float v8 = 0.f;
 #pragma unroll
-              for (int e = 0; e < 8; ++e) ws += D.pjz(zt[e], D.qz(zd[e]));
+              for (int e = 0; e < 8; ++e) v8 += D.pjz(zt[e], D.qz(zd[e]));
+              kahan_add(ws, ws_c, v8);
             }
-            ws = warp_sum(ws);
+            ws = warp_sum(__fsub_rn(ws, ws_c));
             __syncthreads();
             if (lane == 0) s_seg[warp] = (double)ws;
             __syncthreads();

@@ -137,12 +137,6 @@ __device__ __forceinline__ void online_raise(Online &o, float vm, float c) {
 struct OnlineK {
   float m, s, cmp, nbh, nbl;
 };
-__device__ __forceinline__ void kahan_add(float &s, float &cmp, float v) {
-  const float y = __fsub_rn(v, cmp);
-  const float t = __fadd_rn(s, y);
-  cmp = __fsub_rn(__fsub_rn(t, s), y);
-  s = t;
-}
 __device__ __forceinline__ OnlineK onlinek_init() { return {-INFINITY, 0.f, 0.f, 0.f, 0.f}; }
 __device__ __forceinline__ void onlinek_raise(OnlineK &o, float vm, float c) {
   const float nbh = __fmul_rn(-vm, c);

@@ -325,6 +325,13 @@ def test_tree_parity_vocab_128256_rows_from_l2():
     _tree_compare(w, 5)
 
 
+def test_tree_parity_maximum_vocabulary():
+    # V = 2^24 (SV_MAX_V): every pass streams its rows from L2/HBM and a
+    # thread sums tens of thousands of terms per row
+    w = synth.tree(seed=13, B=2, V=1 << 24, levels=(2, 2))
+    _tree_compare(w, 9)
+
+
 def test_tree_chain_equals_sv_verify():
     """A chain tree is linear verification: identical to sv_verify except
     sequences in which the oracle flags a near-tie (counted), and those must
