@@ -40,7 +40,7 @@ def _budget_check(conf, n_req, dc, vc, draft_len=None):
     return gb, r
 
 
-@pytest.mark.parametrize("B,K", [(4, 4), (64, 4), (256, 5), (512, 16), (1024, 7), (1000, 16)])
+@pytest.mark.parametrize("B,K", [(4, 4), (64, 4), (256, 5), (512, 16), (1024, 7), (1000, 16), (1024, 16)])
 def test_budget_parity(B, K):
     conf, dc, vc = synth.budget_inputs(B, K, seed=B + K)
     gb, r = _budget_check(conf, B, dc, vc)
