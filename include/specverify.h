@@ -515,9 +515,9 @@ sv_status_t sv_set_launch_events(void *begin_event, void *end_event);
 
 /* ------------------------------------------------------------------------
  * sv_set_wait_test -- a test hook for failure detection (the pages have no
- * counterpart).  Applies to the later sv_verify, sv_verify_fit and
- * sv_av_score calls made from the calling host thread until it is called
- * again:
+ * counterpart).  Applies to the later sv_verify, sv_verify_fit, sv_av_score
+ * and sv_tts_signal calls made from the calling host thread until it is
+ * called again:
  *   limit_ns  the limit of every device-side wait of their kernels, in ns
  *             (0 = the default, 2 s);
  *   withhold  nonzero: the kernels' producer warps stage no rows, so the
@@ -526,6 +526,10 @@ sv_status_t sv_set_launch_events(void *begin_event, void *end_event);
  *             workspace status reports SV_FLAG_TIMEOUT (sv_status returns
  *             SV_ERR_TIMEOUT) once limit_ns has passed; the device stays
  *             usable, and the next call on the same workspace runs normally.
+ *             sv_tts_signal (rows held in shared memory, i.e. 16-byte
+ *             aligned): no row copy is issued, every out_kl value is NaN and
+ *             out_grad is not written; the kernel for other rows has no
+ *             waits and ignores the hook.
  * For tests of the time-out path only.  Always returns SV_OK.
  * ---------------------------------------------------------------------- */
 sv_status_t sv_set_wait_test(uint64_t limit_ns, int withhold);

@@ -86,6 +86,14 @@ void choose_chunks(int rows, int V, int sms, int &nch, int &chunk_elems) {
 // Failure-detection test hook (sv_set_wait_test): per host thread.
 thread_local unsigned long long t_wait_limit_ns = 0;
 thread_local int t_withhold = 0;
+}  // namespace
+
+void sv::host_wait_test(unsigned long long *limit_ns, int *withhold) {
+  *limit_ns = t_wait_limit_ns;
+  *withhold = t_withhold;
+}
+
+namespace {
 
 void fill_ws(RowPassParams &P, void *ws, const WsLayout &L) {
   unsigned char *w = static_cast<unsigned char *>(ws);

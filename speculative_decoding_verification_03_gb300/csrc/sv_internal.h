@@ -218,6 +218,8 @@ constexpr size_t kAvPartOff = align_up(kAvAccOff + kAvAccDoubles * 8, 256);
 // ---- host helpers shared by the entry points (api.cu) ------------------------
 // SM count of the current device; SV_ERR_UNSUPPORTED unless it is sm_103.
 sv_status_t host_device_info(int *sms);
+// The calling host thread's sv_set_wait_test settings (limit 0 = default).
+void host_wait_test(unsigned long long *limit_ns, int *withhold);
 inline sv_status_t host_cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
 inline bool host_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

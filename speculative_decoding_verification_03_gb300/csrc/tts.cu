@@ -613,6 +613,8 @@ struct GroupArgs {
   int G, S, nb;
   uint32_t gen;         // call generation (tags)
   unsigned char *ws;    // workspace (kTtsWsBytes)
+  unsigned long long wait_ns;  // limit of every wait (2 s, or sv_set_wait_test's)
+  int withhold;         // sv_set_wait_test: no row copies are issued
 };
 
 struct GroupSmem {
@@ -652,18 +654,19 @@ __device__ __forceinline__ void st_word(unsigned long long *p, unsigned long lon
 }
 // Waits of the group kernel poll a barrier between sleeps that double from
 // 32 ns up to max_ns, so a waiting warp leaves its scheduler's issue slots
-// to the warps that compute.  Both are bounded by kTtsWaitNs and set
+// to the warps that compute.  Both are bounded by the launch's limit (2 s,
+// or the one sv_set_wait_test sets) and set
 // SV_FLAG_TIMEOUT when they give up.
 // Chunk copies: also gives up as soon as another thread set the abort flag.
 __device__ __forceinline__ bool wait_copy(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          uint32_t *status, uint32_t max_ns) {
+                                          uint32_t *status, uint32_t max_ns, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t ns = 32;; ns = ns < max_ns ? 2 * ns : max_ns) {
     __nanosleep(ns);
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kTtsWaitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(status, SV_FLAG_TIMEOUT);
       return false;
@@ -672,13 +675,14 @@ __device__ __forceinline__ bool wait_copy(uint64_t *bar, uint32_t parity, volati
 }
 // CTA-local barriers: every arrival on them happens even after an abort, so
 // they always complete; time-bounded only
-__device__ __forceinline__ bool mbar_wait_local(uint64_t *bar, uint32_t parity, uint32_t *status, uint32_t max_ns) {
+__device__ __forceinline__ bool mbar_wait_local(uint64_t *bar, uint32_t parity, uint32_t *status, uint32_t max_ns,
+                                                unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t ns = 32;; ns = ns < max_ns ? 2 * ns : max_ns) {
     __nanosleep(ns);
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kTtsWaitNs) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(status, SV_FLAG_TIMEOUT);
       return false;
     }
@@ -689,7 +693,8 @@ __device__ __forceinline__ bool mbar_wait_local(uint64_t *bar, uint32_t parity, 
 // back-off between polls)
 template <int nw>
 __device__ __forceinline__ bool poll_records(const unsigned long long *rec, int n, int lane, uint32_t tag,
-                                             unsigned long long (&w)[4], uint32_t *status) {
+                                             unsigned long long (&w)[4], uint32_t *status,
+                                             unsigned long long limit_ns) {
   auto load = [&]() {
     if (lane >= n) return true;
     if (nw == 4) {
@@ -709,7 +714,7 @@ __device__ __forceinline__ bool poll_records(const unsigned long long *rec, int 
     if (ns < 1024) ns <<= 1;
     if (!mine) mine = load();
     if (__all_sync(0xffffffffu, mine)) return true;
-    if (__shfl_sync(0xffffffffu, global_ns() - t0 > kTtsWaitNs ? 1 : 0, 0)) {
+    if (__shfl_sync(0xffffffffu, global_ns() - t0 > limit_ns ? 1 : 0, 0)) {
       if (lane == 0) atomicOr(status, SV_FLAG_TIMEOUT);
       return false;
     }
@@ -762,7 +767,7 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks) tts_group_kernel(c
 
   // request chunk ch of the it-th pair of this group into buffer it % nb
   auto issue = [&](int it, int ch) {
-    if (it >= npairs_g) return;
+    if (it >= npairs_g || A.withhold) return;
     const int pair = grp + it * ngroups;
     const int bi = it % nb;
     const int b = pair / K, k = pair - b * K;
@@ -801,7 +806,7 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks) tts_group_kernel(c
       const uint4 *dv = reinterpret_cast<const uint4 *>(ring + (size_t)bi * 2 * slice_bytes + slice_bytes);
       Online ot = lazy_init(), od = lazy_init();
       MinT zmin = E::min_init();
-      if (!*abort_flag) wait_copy(&R.full[bi][cw], (uint32_t)((it / nb) & 1), abort_flag, status, 256u);
+      if (!*abort_flag) wait_copy(&R.full[bi][cw], (uint32_t)((it / nb) & 1), abort_flag, status, 256u, A.wait_ns);
       if (!*abort_flag) pass1_chunk<E, kChunkThreads>(tv, dv, v0, v1, ct, true, c, ot, od, zmin);
       const MS mt = online_final(ot), md = online_final(od);
       R.tstat[it & 1][tid] = make_float4(mt.m, mt.S, md.m, md.S);
@@ -814,7 +819,7 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks) tts_group_kernel(c
       const int pair = grp + it * ngroups;
       const int b = pair / K, k = pair - b * K;
       const int slot = it & (kGrpSlots - 1);
-      mbar_wait_local(&R.const_bar[slot], (uint32_t)((it / kGrpSlots) & 1), status, 256u);
+      mbar_wait_local(&R.const_bar[slot], (uint32_t)((it / kGrpSlots) & 1), status, 256u, A.wait_ns);
       const Pass2Const pk = R.pc[slot];
       const bool ok = R.pc_ok[slot] != 0 && !*abort_flag;
       const bool fast = pass2_fast_ok<E>(pk, zcur);
@@ -844,7 +849,7 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks) tts_group_kernel(c
     // ---------------- coordinator warp
     auto publish = [&](int it) {  // the CTA's entry of pair it
       const float c = pair_c(it);
-      mbar_wait_local(&R.stat_bar[it & 1], (uint32_t)((it >> 1) & 1), status, 512u);
+      mbar_wait_local(&R.stat_bar[it & 1], (uint32_t)((it >> 1) & 1), status, 512u, A.wait_ns);
       // lane l merges the threads l + 32 j, j < 16, as a tree (depth 4)
       constexpr int kPerLane = kGrpCompute / 32;
       MS t[kPerLane], d[kPerLane];
@@ -882,7 +887,8 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks) tts_group_kernel(c
       const int slot = it & (kGrpSlots - 1);
       unsigned long long rw[4];
       const bool got =
-          poll_records<4>(g_stat + ((size_t)slot * kTtsMaxCtas + (size_t)grp * G) * 4, G, lane, tag_of(it), rw, status);
+          poll_records<4>(g_stat + ((size_t)slot * kTtsMaxCtas + (size_t)grp * G) * 4, G, lane, tag_of(it), rw, status,
+                          A.wait_ns);
       MS mt = {-INFINITY, 0.f}, md = {-INFINITY, 0.f};
       if (lane < G) {
         mt = MS{untag(rw[0]), untag(rw[1])};
@@ -899,7 +905,7 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks) tts_group_kernel(c
       }
     };
     auto klsum = [&](int it) {  // the CTA's KL partial of pair it
-      mbar_wait_local(&R.kl_bar[it & 1], (uint32_t)((it >> 1) & 1), status, 512u);
+      mbar_wait_local(&R.kl_bar[it & 1], (uint32_t)((it >> 1) & 1), status, 512u, A.wait_ns);
       constexpr int kPerLane = kGrpCompute / 32;
       float v[kPerLane];
 #pragma unroll
@@ -915,7 +921,7 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks) tts_group_kernel(c
       const int slot = it & (kGrpSlots - 1);
       unsigned long long w[4];
       const bool got = poll_records<1>(g_kl + (size_t)slot * kTtsMaxCtas + (size_t)grp * G, G, lane, tag_of(it), w,
-                                       status);
+                                       status, A.wait_ns);
       const float s = warp_sum(lane < G ? untag(w[0]) : 0.f);
       if (lane == 0) P.out_kl[grp + it * ngroups] = got ? R.scale[slot] * s : __int_as_float(0x7fc00000);
     };
@@ -936,7 +942,7 @@ __global__ void __launch_bounds__(kGrpThreads, kGrpMinBlocks) tts_group_kernel(c
     for (int bi = 0; bi < nb; ++bi)
       for (int ch = 0; ch < kTtsChunks; ++ch)
         if (R.issued[bi][ch])
-          while (!mbar_try_wait(&R.full[bi][ch], (R.issued[bi][ch] - 1u) & 1u) && global_ns() - t0 < kTtsWaitNs) {
+          while (!mbar_try_wait(&R.full[bi][ch], (R.issued[bi][ch] - 1u) & 1u) && global_ns() - t0 < A.wait_ns) {
           }
   }
 }
@@ -1071,7 +1077,11 @@ extern "C" sv_status_t sv_tts_signal(int B, int K, int V, sv_dtype_t dtype, cons
     if (e != cudaSuccess) return host_cuda_status(e);
     uint32_t gen = g_tts_gen.fetch_add(1u) + 1u;
     while ((uint32_t)(gen << 1) == 0u) gen = g_tts_gen.fetch_add(1u) + 1u;  // tag 0 would match a zeroed workspace
-    const GroupArgs A{cfg.G, cfg.S, cfg.nb, gen, static_cast<unsigned char *>(workspace)};
+    unsigned long long wait_ns = 0;
+    int withhold = 0;
+    host_wait_test(&wait_ns, &withhold);
+    const GroupArgs A{cfg.G,  cfg.S,  cfg.nb, gen, static_cast<unsigned char *>(workspace),
+                      wait_ns ? wait_ns : kTtsWaitNs, withhold};
     const unsigned grid = (unsigned)(ngroups * cfg.G);
     if (dtype == SV_BF16) tts_group_kernel<SV_BF16><<<grid, kGrpThreads, cfg.smem, st>>>(P, A);
     else tts_group_kernel<SV_FP32><<<grid, kGrpThreads, cfg.smem, st>>>(P, A);

@@ -225,6 +225,33 @@ def test_tts_masked_logits_and_degenerate_weights():
     _tts_case(w, [1.0, 0.0, -0.5])
 
 
+def test_tts_wait_timeout_is_reported_and_the_next_call_recovers():
+    """A TTS wait that runs out: with sv_set_wait_test's withhold no row copy
+    is issued, so the compute warps' copy waits can only end by their limit
+    (200 us).  The call reports SV_ERR_TIMEOUT through the workspace status,
+    every KL value is NaN and no gradient is written; the next call on the
+    same workspace returns SV_OK and matches the oracle."""
+    dev = torch.device("cuda")
+    w = _tts_rows(4, 2, 32000, torch.bfloat16, 21).to(dev)
+    wt = torch.tensor([1.0, 0.7], dtype=torch.float32, device=dev)
+    ws = binding.tts_workspace(dev)
+    grad = torch.full((w.B, w.K, w.V), 7.0, dtype=torch.bfloat16, device=dev)
+    binding.set_wait_test(limit_ns=200_000, withhold=True)
+    try:
+        kl, _ = binding.tts_signal(w.target, w.draft, w.temperature, wt, out_grad=grad, workspace=ws)
+    finally:
+        binding.set_wait_test(0, False)
+    rc, flags = binding.status(ws)
+    assert rc == 6 and flags & binding.FLAG_TIMEOUT, (rc, flags)  # SV_ERR_TIMEOUT
+    assert bool(torch.isnan(kl).all())
+    assert bool((grad == 7.0).all())  # nothing was written
+    kl2, _ = binding.tts_signal(w.target, w.draft, w.temperature, wt, out_grad=grad, workspace=ws)
+    rc, flags = binding.status(ws)
+    assert rc == 0 and flags == 0, (rc, flags)
+    ref = _tts_case(w, [1.0, 0.7])  # another call, checked against the oracle
+    assert np.array_equal(kl2.cpu().numpy(), ref)  # the launch is deterministic
+
+
 def test_tts_identical_rows_give_zero():
     w = synth.c2(seed=2)
     w.draft = w.target[:, :w.K].contiguous()
