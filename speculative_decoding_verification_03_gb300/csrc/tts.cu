@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kTtsThreads, 1) tts_kernel(const TtsParams P) 
 }
 
 // ---------------------------------------------------------------------------
-// Shared-memory kernels: a group of CTAs shares a row pair, each holding a
+// Shared-memory kernel: a group of CTAs shares a row pair, each holding a
 // slice of both rows in shared memory, so the second pass reads shared
 // memory instead of re-reading the rows.  A slice is loaded by TMA bulk
 // copies in kTtsChunks chunks with one mbarrier each.  Rows must be 16-byte
