@@ -47,6 +47,24 @@ def test_budget_parity(B, K):
     assert 0 < gb <= B * K
 
 
+@pytest.mark.parametrize("B,K", [(200, 8), (1000, 8), (1024, 4), (2000, 8), (8192, 2), (16384, 1)])
+def test_budget_ends_inside_a_tie_group(B, K):
+    # equal confidences: the survivals of one position tie across all
+    # requests, and these cost tables end the budget part-way through a
+    # group, so only the requests with the smallest index keep that position.
+    # The runner-up ratios lie 2e-9 .. 4e-6 below the maximum: inside the
+    # coarse fp32 window, so several candidates reach the fp64 comparison.
+    # Sizes cover every keys-per-thread count of the sort (2, 4, 8, 16) and
+    # the largest table (B*K = 16384, K = 2 without the padded row stride).
+    conf = torch.full((B, K), 0.9)
+    nk = B * K
+    n = np.arange(nk + 1, dtype=np.float64)
+    for q in (0.3, 2.0):
+        vc = torch.from_numpy((B + 0.5 * n + q * n * n / nk).astype(np.float32))
+        gb, r = _budget_check(conf, B, torch.zeros(nk + 1), vc)
+        assert gb == r["budget"] and gb % B != 0, (gb, r["budget"])
+
+
 def test_budget_exact_tie_takes_the_smallest_budget():
     # est / cost is exactly 1 for n = 0, 1, 2: the first maximum, n = 0
     dev = torch.device("cuda")
