@@ -949,7 +949,15 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
         ++nfull[s];
         if (bytes > 0) {
           mbar_arrive_expect_tx(&S.full[s], (uint32_t)bytes);
-          bulk_g2s(S.ring[s], base + (row_off + a0) * kEsz + off_b, (uint32_t)bytes, &S.full[s]);
+          // the first pass's rows (every first target row and draft row, or
+          // every row without early exit) stream through L2 marked evict-first:
+          // they leave L2 to the queued target rows and the draws' re-reads
+          // (C3: 138.2 -> 134.4 us a launch)
+          if (P.lazy && is_target && pos > 0)
+            bulk_g2s(S.ring[s], base + (row_off + a0) * kEsz + off_b, (uint32_t)bytes, &S.full[s]);
+          else
+            bulk_g2s_hint(S.ring[s], base + (row_off + a0) * kEsz + off_b, (uint32_t)bytes, &S.full[s],
+                          policy_evict_first());
         } else {
           mbar_arrive(&S.full[s]);
         }
