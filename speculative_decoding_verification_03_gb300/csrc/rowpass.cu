@@ -949,15 +949,12 @@ __global__ void __launch_bounds__(kRowThreads, 1) rowpass_kernel(const RowPassPa
         ++nfull[s];
         if (bytes > 0) {
           mbar_arrive_expect_tx(&S.full[s], (uint32_t)bytes);
-          // the first pass's rows (every first target row and draft row, or
-          // every row without early exit) stream through L2 marked evict-first:
-          // they leave L2 to the queued target rows and the draws' re-reads
-          // (C3: 138.2 -> 134.4 us a launch)
-          if (P.lazy && is_target && pos > 0)
-            bulk_g2s(S.ring[s], base + (row_off + a0) * kEsz + off_b, (uint32_t)bytes, &S.full[s]);
-          else
-            bulk_g2s_hint(S.ring[s], base + (row_off + a0) * kEsz + off_b, (uint32_t)bytes, &S.full[s],
-                          policy_evict_first());
+          // the rows' statistics read each row once: the copies stream through
+          // L2 marked evict-first, which leaves L2 to the draws (whose rows
+          // are read in parts, and whose crossing sub-chunk is read again by
+          // the final search); C3 138.2 -> 131.5 us a launch
+          bulk_g2s_hint(S.ring[s], base + (row_off + a0) * kEsz + off_b, (uint32_t)bytes, &S.full[s],
+                        policy_evict_first());
         } else {
           mbar_arrive(&S.full[s]);
         }
