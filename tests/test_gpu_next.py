@@ -94,6 +94,19 @@ def test_budget_ragged_ties_and_edges():
     _budget_check(torch.full((3, 4), float("nan")), 3, dc[:13], vc[:13])
 
 
+def test_budget_ragged_edges_sixteen_keys_per_thread():
+    # the same edge mix at B*K = 16000 (16 sort keys per thread): ragged
+    # lengths, a NaN that cuts a request short, rows of zero survivals and
+    # groups of tied survivals
+    conf, dc, vc = synth.budget_inputs(2000, 8, seed=11)
+    conf[::5] = 0.75
+    conf[17, 3] = float("nan")
+    conf[40:60] = 0.0
+    dl = torch.from_numpy(np.random.default_rng(4).integers(0, 9, 2000).astype(np.int32))
+    gb, r = _budget_check(conf, 2000, dc, vc, draft_len=dl)
+    assert 0 < gb < np.count_nonzero(r["est"][1:] > r["est"][:-1])
+
+
 # ----------------------------------------------------------------------------- post-verify
 def _pv_inputs(B, K, seed, cap=48):
     rng = np.random.default_rng(seed)
