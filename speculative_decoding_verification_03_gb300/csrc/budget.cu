@@ -47,19 +47,34 @@ __device__ __forceinline__ uint32_t budget_key(float s) {
 }
 __device__ __forceinline__ float key_survival(uint32_t key) { return __uint_as_float(kInfBits - key); }
 
-// The sort's buffers hold rank i at word i + i / 32.  In a merge round the
-// lanes of a warp read positions about 4 apart, which without the padding
-// word would put lanes 8 apart in one bank; the blocked stores of a thread's
-// E ranks (E <= 16: they never straddle a padding word) are conflict-free
-// too.
-__device__ __forceinline__ int padded(int i) { return i + (i >> 5); }
-__host__ __device__ constexpr int padded_words(int n) { return n + n / 32; }
+// With 16 keys per thread the sort's buffers hold rank i at word i + i / 32:
+// in a merge round the lanes of a warp read positions about 8 apart, which
+// without the padding word would put lanes 4 apart in one bank, and a
+// thread's 16 ranks never straddle a padding word.  With fewer keys per
+// thread the padding's address arithmetic cost more than the conflicts it
+// removes (measured), so ranks sit at their own index.
+template <int E>
+__device__ __forceinline__ int padded(int i) {
+  return E >= 16 ? i + (i >> 5) : i;
+}
+__host__ __device__ constexpr int padded_words(int npad) {  // npad = 1024 E
+  return npad >= 16 * 1024 ? npad + npad / 32 : npad;
+}
 
 template <int E>
 __device__ __forceinline__ void store_blocked(const uint32_t (&r)[E], uint32_t *p) {
-  uint32_t *q = p + padded(threadIdx.x * E);
+  if constexpr (E >= 16) {
+    uint32_t *q = p + padded<E>(threadIdx.x * E);
 #pragma unroll
-  for (int e = 0; e < E; ++e) q[e] = r[e];
+    for (int e = 0; e < E; ++e) q[e] = r[e];
+  } else if constexpr (E % 4 == 0) {
+#pragma unroll
+    for (int v = 0; v < E / 4; ++v)
+      reinterpret_cast<uint4 *>(p + threadIdx.x * E)[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+  } else {
+#pragma unroll
+    for (int v = 0; v < E / 2; ++v) reinterpret_cast<uint2 *>(p + threadIdx.x * E)[v] = make_uint2(r[2 * v], r[2 * v + 1]);
+  }
 }
 template <int W>
 __device__ __forceinline__ void load_words(const uint32_t *p, uint32_t (&c)[W]) {
@@ -79,7 +94,7 @@ __device__ __forceinline__ void load_words(const uint32_t *p, uint32_t (&c)[W]) 
 
 // Ascending sort of npad = 1024 E keys.  On entry r[] holds this thread's E
 // keys (any order); on exit thread t holds ranks t E .. t E + E - 1 in r[]
-// and keys[] the sorted array, rank i at padded(i).  tmp: padded_words(npad)
+// and keys[] the sorted array, rank i at padded<E>(i).  tmp: padded_words(npad)
 // words of scratch.
 //   (a) every warp sorts the 32 E keys of its threads: a bitonic network,
 //       strides below E inside a thread, strides E .. 16 E through shuffles;
@@ -128,21 +143,21 @@ __device__ void block_sort(uint32_t (&r)[E], uint32_t *keys, uint32_t *tmp) {
     int lo = diag > L ? diag - L : 0, hi = diag < L ? diag : L;
     while (lo < hi) {  // i = how many of the first diag outputs come from A
       const int mid = (lo + hi) >> 1;
-      if (src[padded(a0 + mid)] <= src[padded(b0 + diag - 1 - mid)]) lo = mid + 1;
+      if (src[padded<E>(a0 + mid)] <= src[padded<E>(b0 + diag - 1 - mid)]) lo = mid + 1;
       else hi = mid;
     }
     int i = lo, j = diag - lo;
-    uint32_t a = i < L ? src[padded(a0 + i)] : 0u, b = j < L ? src[padded(b0 + j)] : 0u;
+    uint32_t a = i < L ? src[padded<E>(a0 + i)] : 0u, b = j < L ? src[padded<E>(b0 + j)] : 0u;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const bool take_a = i < L && (j >= L || a <= b);
       r[e] = take_a ? a : b;
       if (take_a) {
         ++i;
-        a = i < L ? src[padded(a0 + i)] : 0u;
+        a = i < L ? src[padded<E>(a0 + i)] : 0u;
       } else {
         ++j;
-        b = j < L ? src[padded(b0 + j)] : 0u;
+        b = j < L ? src[padded<E>(b0 + j)] : 0u;
       }
     }
     store_blocked(r, dst);
@@ -212,7 +227,7 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const Budg
   const int B = P.B, K = P.K, NK = B * K, npad = P.npad, S = P.stride;
 
   const int nw = padded_words(npad);
-  uint32_t *keys = smem;                          // [nw] sort input, then the ranked keys (rank i at padded(i))
+  uint32_t *keys = smem;                          // [nw] sort input, then the ranked keys (rank i at padded<E>(i))
   uint32_t *tmp = smem + nw;                      // [nw] the sort's scratch, then
   float *costr = reinterpret_cast<float *>(tmp);  //      the cost of n = rank + 1 drafts (unpadded)
   uint32_t *cfk = smem + 2 * nw;                  // [B][S] confidences, then the keys by (b, i)
@@ -386,11 +401,11 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const Budg
   uint32_t kth = 0;
   int need = 0;
   if (budget > 0) {
-    kth = keys[padded(budget - 1)];
+    kth = keys[padded<E>(budget - 1)];
     int lo = 0, hi = budget - 1;  // first rank holding kth
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (keys[padded(mid)] < kth) lo = mid + 1;
+      if (keys[padded<E>(mid)] < kth) lo = mid + 1;
       else hi = mid;
     }
     need = budget - lo;
