@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(kBudgetThreads, 1) av_budget_kernel(const Budg
   // 2. the ranking
   uint32_t r[E];
   {
-    uint32_t c[E % 4 == 0 ? 4 : 2];
-    constexpr int W = E % 4 == 0 ? 4 : 2;
+    constexpr int W = E % 4 == 0 ? 4 : 2;  // words per vector load
+    uint32_t c[W];
 #pragma unroll
     for (int v = 0; v < E / W; ++v) {
       load_words(keys + tid * E + v * W, c);
